@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Benchmark of libfattn on one GB300 (or N independent replicas).
+
+One step = one fused attention forward through the C ABI on the workload the
+headline metric is quoted on: bf16, B=2, H=32, N=M=8192, d=128, causal
+(FLOPs = 4*B*H*N*M*d / 2).  Inputs (403 MB) are larger than the 129 MB L2, so
+no flush is needed between steps.  The row-softmax workload (bf16
+[4096, 32768], one read + one write, 537 MB) is the second headline and is
+timed in its own loop on the same device; the LSE-only kernel and the fp32
+attention path are timed alongside for completeness.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on a bounded sample of the same workload instead (the reference arm).
+Multi-GPU: every rank runs the full workload on its own GPU (weak scaling, no
+collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak; row-softmax GB/s vs HBM"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world_size: int, device=None) -> float:
+    """Max of a float over all ranks (identity when world_size == 1)."""
+    if world_size <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, world_size: int, max_seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
+    return units_per_rank * world_size / max_seconds
+
+
+def barrier(world_size: int):
+    if world_size > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        self.out.flush()
+        with open(self.out.name) as f:
+            lines = [l.strip() for l in f if l.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        # samples under load: the upper half by power draw
+        cut = statistics.median(power)
+        loaded = [s for s, p in zip(sm, power) if p >= cut] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+def gpu_uuid():
+    try:
+        import torch
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ timing
+def time_launches(fn, steps: int, warmup: int, world_size: int):
+    """Warm up, then time `steps` calls of fn() with CUDA events on the current
+    stream: returns (total seconds, max over ranks; mean per-launch seconds)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world_size)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start.record(stream)
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world_size)
+    total = start.elapsed_time(end) / 1e3
+    per = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+    return max_over_ranks(total, world_size, device="cuda"), per
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_oracle_sample(w, target_s: float = 10.0, max_rows: int | None = None):
+    """Time the fp64 oracle on a seeded sample of the workload's query rows.
+    Returns (TFLOP/s by the workload's FLOP convention, seconds, rows, threads)."""
+    import numpy as np
+    import oracle
+    from online_softmax_10_gb300 import inputs
+    q, k, v = inputs.workload_attn_inputs(w)
+    Q, K, V = oracle.as_f64(q), oracle.as_f64(k), oracle.as_f64(v)
+    threads = oracle.default_threads()
+    total_rows = w.B * w.H * w.N
+
+    def flops(rows):
+        i = rows % w.N
+        kept = np.minimum(i + 1, w.M) if w.causal else np.full_like(i, w.M)
+        return float(np.sum(4.0 * kept * w.d))
+
+    probe = inputs.sample_rows(total_rows, 256, seed=99).numpy()
+    t0 = time.perf_counter()
+    oracle.attn_fwd(Q, K, V, w.scale, w.causal, rows=probe, nthreads=threads)
+    tp = time.perf_counter() - t0
+    n = int(len(probe) * target_s / max(tp, 1e-3))
+    n = max(256, min(n, total_rows if max_rows is None else max_rows))
+    rows = inputs.sample_rows(total_rows, n, seed=100).numpy()
+    t0 = time.perf_counter()
+    oracle.attn_fwd(Q, K, V, w.scale, w.causal, rows=rows, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return flops(rows) / dt / 1e12, dt, len(rows), threads, flops(rows)
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, world_size, rank):
+    """The reference arm: the fp64 CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    from online_softmax_10_gb300 import inputs
+    import numpy as np
+    import oracle
+    w = inputs.ATTN_B2H32_8192_D128_CAUSAL
+    q, k, v = inputs.workload_attn_inputs(w)
+    Q, K, V = oracle.as_f64(q), oracle.as_f64(k), oracle.as_f64(v)
+    threads = oracle.default_threads()
+    total_rows = w.B * w.H * w.N
+    # size one step so that warmup + steps stay within about two minutes
+    probe = inputs.sample_rows(total_rows, 128, seed=99).numpy()
+    t0 = time.perf_counter()
+    oracle.attn_fwd(Q, K, V, w.scale, w.causal, rows=probe, nthreads=threads)
+    tp = time.perf_counter() - t0
+    per_step_target = min(10.0, 120.0 / max(1, args.steps + args.warmup))
+    n = max(64, min(total_rows, int(len(probe) * per_step_target / max(tp, 1e-3))))
+    samples = [inputs.sample_rows(total_rows, n, seed=1000 + s).numpy() for s in range(args.warmup + args.steps)]
+
+    def fl(rows):
+        i = rows % w.N
+        return float(np.sum(4.0 * np.minimum(i + 1, w.M) * w.d))
+
+    for s in range(args.warmup):
+        oracle.attn_fwd(Q, K, V, w.scale, w.causal, rows=samples[s], nthreads=threads)
+    t0 = time.perf_counter()
+    work = 0.0
+    for s in range(args.warmup, args.warmup + args.steps):
+        oracle.attn_fwd(Q, K, V, w.scale, w.causal, rows=samples[s], nthreads=threads)
+        work += fl(samples[s])
+    dt = time.perf_counter() - t0
+    value = work / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "M": w.M, "d": w.d, "causal": w.causal,
+                   "sample_rows_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} seeded query rows of {total_rows} per step (fp64, three-pass softmax)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world_size, rank, local_rank):
+    import torch
+    from online_softmax_10_gb300 import build as fbuild
+    from online_softmax_10_gb300 import fattn, inputs
+
+    torch.cuda.set_device(local_rank)
+    fbuild.build()
+    peaks, peak_src = load_peaks()
+    w = inputs.ATTN_B2H32_8192_D128_CAUSAL
+    q_h, k_h, v_h = inputs.workload_attn_inputs(w)
+    q, k, v = q_h.cuda(), k_h.cuda(), v_h.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+
+    def step():
+        fattn.attn_fwd(q, k, v, w.scale, w.causal, out=o, lse=lse)
+
+    step()
+    assert fattn.device_status() == fattn.FA_OK
+    with ClockSampler(gpu_uuid()) as clk:
+        total_s, per_launch_s = time_launches(step, args.steps, args.warmup, world_size)
+    clocks = clk.summary()
+    assert fattn.device_status() == fattn.FA_OK
+    flops = w.flops()
+    value = aggregate_throughput(flops, world_size, total_s / args.steps) / 1e12
+    achieved = flops / per_launch_s / 1e12
+
+    # ---- end to end through the public API with host buffers
+    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+    op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        qd.copy_(qp, non_blocking=True)
+        kd.copy_(kp, non_blocking=True)
+        vd.copy_(vp, non_blocking=True)
+        fattn.attn_fwd(qd, kd, vd, w.scale, w.causal, out=o, lse=lse)
+        op.copy_(o, non_blocking=True)
+        lp.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 30))
+    e2e_total, _ = time_launches(e2e_step, e2e_steps, 2, world_size)
+    e2e_value = aggregate_throughput(flops, world_size, e2e_total / e2e_steps) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    del qd, kd, vd, qp, kp, vp
+
+    # ---- row softmax workload (second headline): bf16 [4096, 32768] -> bf16 P + fp32 LSE
+    rw = inputs.ROWS_4096x32768
+    x = inputs.workload_rows_inputs(rw).cuda()
+    p = torch.empty_like(x)
+    plse = torch.empty(rw.rows, dtype=torch.float32, device="cuda")
+    rsteps = max(20, min(400, args.steps * 2))
+    r_total, r_per = time_launches(lambda: fattn.softmax_rows(x, out=p, lse=plse), rsteps, max(3, args.warmup),
+                                   world_size)
+    r_bytes = rw.rows * rw.cols * 2 * 2 + rw.rows * 4
+    r_gbs = r_bytes / r_per / 1e9
+    l_total, l_per = time_launches(lambda: fattn.logsumexp_rows(x, out=plse), rsteps, 3, world_size)
+    l_bytes = rw.rows * rw.cols * 2 + rw.rows * 4
+    del x, p
+
+    # ---- fp32 attention workload (N = M = 64, d = 64): launch-latency bound
+    fw = inputs.ATTN_F32_64
+    fq, fk, fv = (t.cuda() for t in inputs.workload_attn_inputs(fw))
+    f_total, f_per = time_launches(lambda: fattn.attn_fwd(fq, fk, fv, fw.scale, fw.causal), 200, 10, world_size)
+    assert fattn.device_status() == fattn.FA_OK
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, dt, nrows, threads, _ = cpu_oracle_sample(w, target_s=args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{nrows} seeded query rows of {w.B * w.H * w.N} ({dt:.1f} s, fp64 three-pass softmax, "
+                         f"FLOPs by the same 4*kept*d convention)"}
+
+    peak_t = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world_size, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "M": w.M, "d": w.d, "causal": w.causal,
+                   "inputs": "Q,K,V i.i.d. N(0,1) seed 3, bf16", "l2": "inputs 403 MB > 129 MB L2, no flush",
+                   "parallelism": f"replicas x{world_size}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": achieved / peak_t, "traffic": args.traffic,
+                     "peak_source": f"bf16_tflops (burst), {peak_src}"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "row_softmax": {"workload": rw.name, "value": r_gbs, "unit": "GB/s", "us_per_launch": r_per * 1e6,
+                        "roofline": {"bound": "hbm", "achieved": r_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                     "frac": r_gbs / peaks["hbm_gbs"], "traffic": args.rows_traffic,
+                                     "bytes_per_launch": r_bytes, "peak_source": f"hbm_gbs, {peak_src}"},
+                        "launches": rsteps, "l2": "input 268 MB > 129 MB L2, no flush"},
+        "logsumexp_rows": {"workload": rw.name, "value": l_bytes / l_per / 1e9, "unit": "GB/s",
+                           "us_per_launch": l_per * 1e6, "frac": l_bytes / l_per / 1e9 / peaks["hbm_gbs"]},
+        "attn_f32": {"workload": fw.name, "us_per_launch": f_per * 1e6,
+                     "value": fw.flops() / f_per / 1e12, "unit": "TFLOP/s"},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per attention launch, if captured for the current kernel")
+    ap.add_argument("--rows-traffic", type=float, default=None,
+                    help="ncu dram bytes per row-softmax launch, if captured for the current kernel")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world_size, rank, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world_size, rank)
+        return
+    if world_size > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, world_size, rank, local_rank)
+    finally:
+        if world_size > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,145 @@
+/*
+ * fattn.h -- C ABI of libfattn: exact attention forward with the online-softmax
+ * recurrence, and row-wise online softmax / log-sum-exp, for NVIDIA GB300
+ * (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or retains device memory, and never reads host
+ *    memory through these pointers.
+ *  - Every pointer must be 16-byte aligned (FA_ERR_MISALIGNED otherwise).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls are asynchronous: they validate, enqueue and return.  A
+ *    launch failure is reported as FA_ERR_CUDA; nothing is synchronised.
+ *  - Argument errors are detected before anything is enqueued; on any non-OK
+ *    status no output has been written.
+ *  - dtype codes: FA_F32 (IEEE binary32) and FA_BF16 (bfloat16).  All
+ *    arithmetic inside the kernels is fp32; bf16 stores round to nearest even.
+ *  - LSE is always fp32 and in natural-log units.
+ *  - Device kernels never spin without a bound.  A wait that exceeds its bound
+ *    makes the kernel give up, leave its outputs incomplete and record
+ *    FA_ERR_DEVICE_TIMEOUT in a per-device status word that
+ *    fa_device_status() returns.
+ *  - Re-entrant; the only global state is per-device kernel attributes and the
+ *    device status word.
+ */
+#ifndef FATTN_H
+#define FATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_dtype {
+    FA_F32 = 0,
+    FA_BF16 = 1
+} fa_dtype;
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, overflow  */
+    FA_ERR_UNSUPPORTED = 2,     /* valid but not implemented (dtype, head dim) */
+    FA_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned           */
+    FA_ERR_CUDA = 4,            /* the CUDA runtime reported an error         */
+    FA_ERR_DEVICE_TIMEOUT = 5   /* a kernel's bounded wait ran out            */
+} fa_status;
+
+#define FA_VERSION 100  /* 1.0.0 */
+
+/*
+ * fa_attn_fwd -- O = softmax(scale * Q K^T [+ causal mask]) V and the per-row
+ * log-sum-exp of the scaled, masked scores, in one fused pass.
+ *
+ * Defined by: "什么是 online softmax and flash attention", section
+ * "Attention的数学表达", eq (8)-(9) (shapes Q[N,K], K[M,K], V[M,K], A[N,K]
+ * with K the head dimension), computed by the block-wise online merge of the
+ * running max m, normaliser l and unnormalised output o~ given on
+ * "从原始Softmax到在线Softmax", section on the block-wise online softmax
+ * (o = o~ / l after the last key block); LSE as defined on the same page,
+ * section "softmax形式推导".
+ *
+ *   Q    [B, H, N, d]  row-major, d fastest, dtype in_dtype
+ *   K    [B, H, M, d]  row-major, dtype in_dtype
+ *   V    [B, H, M, d]  row-major, dtype in_dtype
+ *   O    [B, H, N, d]  row-major, dtype out_dtype (written)
+ *   LSE  [B, H, N]     fp32, natural log of sum_j exp(scale * q_i . k_j) over
+ *                      the keys kept for row i (written; may be NULL = skip)
+ *   scale  multiplier of Q K^T (finite, non-zero), usually 1/sqrt(d)
+ *   causal 0: every key is kept; 1: key j is kept for query i iff j <= i
+ *          (top-left aligned, also when N != M)
+ *   in_dtype / out_dtype:
+ *      FA_BF16 in  -> tensor-core path, d in {64, 128}; out FA_BF16 or FA_F32
+ *      FA_F32  in  -> fp32 CUDA-core path, d in {16, 32, 64, 128}; out FA_F32
+ * Errors: FA_ERR_INVALID_ARG for NULL Q/K/V/O, B,H,N,M,d <= 0, a non-finite or
+ * zero scale, or sizes whose element count overflows; FA_ERR_UNSUPPORTED for
+ * other dtype / d combinations; FA_ERR_MISALIGNED; FA_ERR_CUDA.
+ */
+int fa_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                int B, int H, int N, int M, int d, float scale, int causal,
+                int in_dtype, int out_dtype, void* stream);
+
+/*
+ * fa_softmax_rows -- P[r, :] = softmax(X[r, :]) and LSE[r] = log sum_c exp X[r, c]
+ * for every row, reading X from memory once when a row fits on chip
+ * (cols <= 65536 for bf16, <= 32768 for fp32) and twice otherwise.
+ *
+ * Defined by: "从原始Softmax到在线Softmax", section "softmax形式推导" (stable
+ * softmax, log-sum-exp), computed with the online normaliser of
+ * "什么是 online softmax and flash attention", section "Online softmax",
+ * eq (3)-(7), merged across threads with the pairwise form of the same update.
+ *
+ *   X    [rows, cols]  row-major, dtype in_dtype (FA_BF16 or FA_F32)
+ *   P    [rows, cols]  row-major, dtype out_dtype (FA_BF16 or FA_F32), written;
+ *                      must not be NULL (it may alias X when the dtypes match)
+ *   LSE  [rows]        fp32, written; may be NULL = skip
+ * Errors: FA_ERR_INVALID_ARG for NULL X/P, rows <= 0, cols <= 0, or
+ * rows*cols overflowing; FA_ERR_UNSUPPORTED for other dtypes;
+ * FA_ERR_MISALIGNED; FA_ERR_CUDA.
+ */
+int fa_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols,
+                    int in_dtype, int out_dtype, void* stream);
+
+/*
+ * fa_logsumexp_rows -- LSE[r] = log sum_c exp X[r, c], one read of X.
+ *
+ * Defined by: "从原始Softmax到在线Softmax", section "softmax形式推导" (the
+ * LSE(z) definition), computed with the online normaliser of
+ * "什么是 online softmax and flash attention", section "Online softmax".
+ *
+ *   X    [rows, cols]  row-major, dtype in_dtype (FA_BF16 or FA_F32)
+ *   LSE  [rows]        fp32, written; must not be NULL
+ * Errors: as fa_softmax_rows.
+ */
+int fa_logsumexp_rows(const void* X, float* LSE, long rows, long cols,
+                      int in_dtype, void* stream);
+
+/*
+ * fa_device_status -- synchronise `stream`, then return FA_OK or the first
+ * error a kernel recorded on the current device since the last reset
+ * (FA_ERR_DEVICE_TIMEOUT), or FA_ERR_CUDA if the synchronisation itself
+ * failed.  reset != 0 clears the recorded status.  (No counterpart on the
+ * pages: this is the library's failure-detection hook.)
+ */
+int fa_device_status(void* stream, int reset);
+
+/*
+ * fa_selftest_wait_timeout -- launch one CTA that waits on a barrier nothing
+ * ever completes, with a bound of `limit_us` microseconds (1..1000000), then
+ * return fa_device_status(stream, 1).  Expected result: FA_ERR_DEVICE_TIMEOUT
+ * with the CUDA context still usable.  Exercises the same bounded-wait code
+ * every pipelined kernel uses.  (No counterpart on the pages.)
+ */
+int fa_selftest_wait_timeout(int limit_us, void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* fa_status_string(int status);
+
+/* FA_VERSION of the built library. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H */

@@ -1,0 +1,9 @@
+"""libfattn for NVIDIA GB300 (sm_103a): exact attention forward with the
+online-softmax recurrence, and row-wise online softmax / log-sum-exp.
+
+The compute path is the C-ABI library ``libfattn.so`` (include/fattn.h), built
+in-tree by :mod:`online_softmax_10_gb300.build`; :mod:`.fattn` is its thin
+binding.  :mod:`.inputs` holds the seeded synthetic input generators.
+"""
+from .fattn import (FattnError, attn_fwd, device_status, logsumexp_rows, selftest_wait_timeout,  # noqa: F401
+                    softmax_rows, status_string, version)

@@ -1,0 +1,435 @@
+// attn_tc.cu -- bf16 attention forward on the 5th-generation tensor cores.
+//
+// O = softmax(scale * Q K^T [+ causal mask]) V and the per-row LSE, bf16 inputs,
+// fp32 accumulation, in one fused pass that never writes the score matrix to
+// memory.  The arithmetic is the block-wise online merge of
+// "从原始Softmax到在线Softmax" (section on the block-wise online softmax):
+// for each key block j,
+//     m' = max(m, max_k s_k),
+//     o~ <- e^{m-m'} o~ + sum_k e^{s_k-m'} v_k,     l <- e^{m-m'} l + sum_k e^{s_k-m'},
+// and o = o~ / l after the last block; LSE = m + log l ("softmax形式推导").
+// The loop order is query-tile outer, key-tile inner (the ordering the
+// "Softmax与Flash-Attention" page attributes to FlashAttention-2), so o~
+// stays on chip for the whole pass.
+//
+// CTA organisation (one CTA per 256 query rows of one (batch, head)):
+//   warps 0-3  softmax warpgroup for Q tile 0 (rows q0 .. q0+127), one row per thread
+//   warps 4-7  softmax warpgroup for Q tile 1 (rows q0+128 .. q0+255)
+//   warp  8    TMA producer: Q tiles once, then a ring of K and V tiles
+//   warp  9    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+// Tensor memory (512 columns x 128 lanes of 32 bit):
+//   S_0 [0,128)  S_1 [128,256)  O_0 [256,256+D)  O_1 [256+D,256+2D)
+// P_t (bf16, two per column) overwrites the first 64 columns of S_t and is the
+// A operand of the P V product straight from tensor memory.
+// The two softmax warpgroups ping-pong: while one exponentiates, the tensor
+// core runs the other tile's P V and next Q K^T.
+//
+// Numerics: scores are moved to base 2 (scale * log2 e is folded into the
+// exponent's FMA).  The running max is only raised when a block's max exceeds
+// it by more than 8 (base-2 units); otherwise the stale max stays the
+// reference, which keeps every p <= 2^8 and is exact because l and o~ share
+// the reference.  P is rounded to bf16 for the tensor core; l sums the fp32 p.
+//
+// Every wait is bounded (see ptx.cuh); on a timeout the CTA records the error
+// in the device status word, drains its own TMA copies and MMAs, frees its
+// tensor memory and exits.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "fattn_internal.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;           // query rows per Q tile
+constexpr int BN = 128;           // keys per K/V tile
+constexpr int kThreads = 320;     // 10 warps
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.f;  // base-2 units
+constexpr uint32_t kAtomBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzle atom of a tile
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct Cfg {
+    static constexpr int kAtoms = D / 64;                        // 128-byte column blocks per row
+    static constexpr uint32_t kTileBytes = (uint32_t)BM * D * 2; // one 128-row bf16 tile
+    static constexpr int NST = D == 128 ? 2 : 4;                 // K/V ring depth
+    static constexpr uint32_t kQ = 0;                            // Q_0, Q_1
+    static constexpr uint32_t kK = 2 * kTileBytes;               // K ring
+    static constexpr uint32_t kV = kK + NST * kTileBytes;        // V ring
+    static constexpr uint32_t kBar = kV + NST * kTileBytes;      // mbarriers
+    static constexpr int kNumBars = 9 + 4 * NST;
+    static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kSmemBytes = kAbort + 4 + 1024;    // + slack to align the base
+    // barrier indices
+    __host__ __device__ static constexpr int QF(int t) { return t; }
+    __host__ __device__ static constexpr int KF(int s) { return 2 + s; }
+    __host__ __device__ static constexpr int KE(int s) { return 2 + NST + s; }
+    __host__ __device__ static constexpr int VF(int s) { return 2 + 2 * NST + s; }
+    __host__ __device__ static constexpr int VE(int s) { return 2 + 3 * NST + s; }
+    __host__ __device__ static constexpr int SF(int t) { return 2 + 4 * NST + t; }
+    __host__ __device__ static constexpr int PF(int t) { return 4 + 4 * NST + t; }
+    __host__ __device__ static constexpr int OD(int t) { return 6 + 4 * NST + t; }
+    static constexpr int DRAIN = 8 + 4 * NST;
+    // tensor-memory columns
+    __host__ __device__ static constexpr uint32_t colS(int t) { return (uint32_t)t * 128u; }
+    __host__ __device__ static constexpr uint32_t colO(int t) { return 256u + (uint32_t)t * D; }
+};
+static_assert(Cfg<128>::kSmemBytes <= 227 * 1024, "smem budget (d=128)");
+static_assert(Cfg<64>::kSmemBytes <= 227 * 1024, "smem budget (d=64)");
+
+// Number of key tiles Q tile t of the CTA starting at query row q0 must visit.
+template <bool CAUSAL>
+__device__ __forceinline__ int kv_tiles_for(int q0, int t, int N, int M) {
+    const int first = q0 + t * BM;
+    if (first >= N) return 0;
+    const int nM = (M + BN - 1) / BN;
+    if (!CAUSAL) return nM;
+    const int last = min(N, first + BM) - 1;
+    return min(nM, last / BN + 1);
+}
+
+__device__ __forceinline__ void record_failure(volatile int* abort_flag, int* status) {
+    *abort_flag = 1;
+    atomicExch(status, kDevStatusTimeout);
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, void* __restrict__ O, float* __restrict__ LSE,
+                    int N, int M, float c_log2, int out_bf16, int* status) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kAbort);
+    const uint32_t* tmem_slot = reinterpret_cast<const uint32_t*>(gbase + C::kTmemSlot);
+    auto bar = [&](int i) -> uint32_t { return base + C::kBar + 8u * (uint32_t)i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long bh = blockIdx.y;
+    const int qblk = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;  // longest first
+    const int q0 = qblk * 2 * BM;
+    const int n0 = kv_tiles_for<CAUSAL>(q0, 0, N, M);
+    const int n1 = kv_tiles_for<CAUSAL>(q0, 1, N, M);
+    const int nk = max(n0, n1);
+
+    // ------------------------------------------------------------ set-up
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kNumBars; ++i) {
+            uint32_t count = 1;
+            if (i == C::PF(0) || i == C::PF(1)) count = BM;  // one arrival per softmax thread
+            mbar_init(bar(i), count);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(base + C::kTmemSlot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kLoadWarp) {
+        // -------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol_q = l2_policy_evict_first();
+            for (int t = 0; t < 2; ++t) {
+                if ((t == 0 ? n0 : n1) == 0) continue;
+                mbar_expect_tx(bar(C::QF(t)), C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d_hint(base + C::kQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar(C::QF(t)),
+                                     a * 64, q0 + t * BM, (int)bh, pol_q);
+            }
+            int issued_k = 0, issued_v = 0;
+            for (int j = 0; j < nk; ++j) {
+                const int s = j % C::NST;
+                const uint32_t ph = (uint32_t)(j / C::NST) & 1u;
+                if (!mbar_wait_bounded(bar(C::KE(s)), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                    record_failure(abort_flag, status);
+                    break;
+                }
+                mbar_expect_tx(bar(C::KF(s)), C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(base + C::kK + s * C::kTileBytes + a * kAtomBytes, &tmK, bar(C::KF(s)),
+                                a * 64, j * BN, (int)bh);
+                issued_k = j + 1;
+                if (!mbar_wait_bounded(bar(C::VE(s)), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                    record_failure(abort_flag, status);
+                    break;
+                }
+                mbar_expect_tx(bar(C::VF(s)), C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(base + C::kV + s * C::kTileBytes + a * kAtomBytes, &tmV, bar(C::VF(s)),
+                                a * 64, j * BN, (int)bh);
+                issued_v = j + 1;
+            }
+            // Drain: the last copy issued into each stage has landed before the
+            // CTA may exit (returns at once on the normal path, where every
+            // copy has been consumed).
+            for (int j = max(0, issued_k - C::NST); j < issued_k; ++j)
+                mbar_wait_bounded(bar(C::KF(j % C::NST)), (uint32_t)(j / C::NST) & 1u, nullptr, kWaitLimitNs);
+            for (int j = max(0, issued_v - C::NST); j < issued_v; ++j)
+                mbar_wait_bounded(bar(C::VF(j % C::NST)), (uint32_t)(j / C::NST) & 1u, nullptr, kWaitLimitNs);
+            for (int t = 0; t < 2; ++t)
+                if ((t == 0 ? n0 : n1) > 0) mbar_wait_bounded(bar(C::QF(t)), 0, nullptr, kWaitLimitNs);
+        }
+    } else if (warp == kMmaWarp) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
+            constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);    // P from TMEM, V MN-major
+            const int nt[2] = {n0, n1};
+            auto issue_S = [&](int t, int s) {
+                const uint32_t qa = base + C::kQ + t * C::kTileBytes;
+                const uint32_t kb = base + C::kK + s * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kAtomBytes + (uint32_t)(kk & 3) * 32u;
+                    mma_ss(tmem + C::colS(t), umma_desc_sw128(qa + off, 16, 1024), umma_desc_sw128(kb + off, 16, 1024),
+                           idS, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_PV = [&](int t, int s, bool acc) {
+                const uint32_t vb = base + C::kV + s * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    mma_ts(tmem + C::colO(t), tmem + C::colS(t) + (uint32_t)kk * 8u,
+                           umma_desc_sw128(vb + (uint32_t)kk * 2048u, kAtomBytes, 1024), idO,
+                           (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = true;
+            for (int t = 0; t < 2 && ok; ++t)
+                if (nt[t] > 0) ok = mbar_wait_bounded(bar(C::QF(t)), 0, abort_flag, kWaitLimitNs);
+            if (ok) ok = mbar_wait_bounded(bar(C::KF(0)), 0, abort_flag, kWaitLimitNs);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < 2; ++t) {
+                    if (nt[t] == 0) continue;
+                    issue_S(t, 0);
+                    mma_commit(bar(C::SF(t)));
+                }
+                mma_commit(bar(C::KE(0)));
+            }
+            for (int j = 0; j < nk && ok; ++j) {
+                const int s = j % C::NST;
+                const uint32_t ph = (uint32_t)(j / C::NST) & 1u;
+                const int jn = j + 1;
+                const int sn = jn % C::NST;
+                const uint32_t phn = (uint32_t)(jn / C::NST) & 1u;
+                bool kn_ready = false;
+                if (!(ok = mbar_wait_bounded(bar(C::VF(s)), ph, abort_flag, kWaitLimitNs))) break;
+                tc_fence_after();
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= nt[t]) continue;
+                    if (!(ok = mbar_wait_bounded(bar(C::PF(t)), (uint32_t)j & 1u, abort_flag, kWaitLimitNs))) break;
+                    tc_fence_after();
+                    issue_PV(t, s, j > 0);
+                    if (j == nt[t] - 1) mma_commit(bar(C::OD(t)));
+                    if (jn < nt[t]) {
+                        if (!kn_ready) {
+                            if (!(ok = mbar_wait_bounded(bar(C::KF(sn)), phn, abort_flag, kWaitLimitNs))) break;
+                            tc_fence_after();
+                            kn_ready = true;
+                        }
+                        issue_S(t, sn);
+                        mma_commit(bar(C::SF(t)));
+                    }
+                }
+                mma_commit(bar(C::VE(s)));
+                if (kn_ready) mma_commit(bar(C::KE(sn)));
+            }
+            if (!ok) record_failure(abort_flag, status);
+            // Drain: every MMA issued above has completed before TMEM is freed.
+            mma_commit(bar(C::DRAIN));
+            mbar_wait_bounded(bar(C::DRAIN), 0, nullptr, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------- softmax warpgroups
+        const int t = warp >> 2;          // Q tile
+        const int wq = warp & 3;          // TMEM lane quarter of this warp
+        const int row = wq * 32 + lane;   // row within the tile
+        const int qi = q0 + t * BM + row; // query index
+        const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
+        const uint32_t tS = tl + C::colS(t);
+        const uint32_t tO = tl + C::colO(t);
+        const int n = t == 0 ? n0 : n1;
+        float m = -CUDART_INF_F;  // running max (base-2 units), possibly stale by < 8
+        float l = 0.f;            // running sum of p relative to m
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            ok = mbar_wait_bounded(bar(C::SF(t)), (uint32_t)j & 1u, abort_flag, kWaitLimitNs);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[128];
+            tmem_ld_x128(tS, sr);
+            float sv[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
+            const int k0 = j * BN;
+            const bool need_mask = (k0 + BN > M) || (CAUSAL && k0 + BN - 1 > q0 + t * BM);
+            if (need_mask) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int key = k0 + c;
+                    if (key >= M || (CAUSAL && key > qi)) sv[c] = -CUDART_INF_F;
+                }
+            }
+            float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+            for (int c = 4; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c_log2;
+            float alpha = 1.f;
+            bool rescale = false;
+            if (j == 0) {
+                m = m_tile;
+            } else {
+                const float m_cand = fmaxf(m, m_tile);
+                if (m_cand - m > kRescaleThreshold) {
+                    alpha = ex2(m - m_cand);
+                    m = m_cand;
+                    rescale = true;
+                }
+            }
+            // p = 2^(s * scale * log2e - m); P (bf16) overwrites S in tensor memory
+            const float neg_m = m == -CUDART_INF_F ? 0.f : -m;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = ex2(fmaf(sv[2 * c], c_log2, neg_m));
+                const float p1 = ex2(fmaf(sv[2 * c + 1], c_log2, neg_m));
+                ls[c & 3] += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l = fmaf(l, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+            tmem_st_x64(tS, pk);
+            // o~ <- alpha o~ when the reference max was raised.  The previous
+            // P V of this tile has completed: it was issued before the Q K^T
+            // whose completion this warpgroup just waited for.
+            if (__any_sync(0xFFFFFFFFu, rescale)) {
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld_x32(tO + ch * 32, r);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+                    tmem_st_x32(tO + ch * 32, r);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(C::PF(t)));
+        }
+        // ------------------------------------------------------ epilogue
+        if (n > 0 && ok) {
+            ok = mbar_wait_bounded(bar(C::OD(t)), 0, abort_flag, kWaitLimitNs);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (ok) {
+                tc_fence_after();
+                const float inv_l = 1.f / l;
+                const bool store = qi < N;
+                const long orow = bh * (long)N + qi;
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld_x32(tO + ch * 32, r);
+                    if (!store) continue;
+                    if (out_bf16) {
+                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(O) + orow * D + ch * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * e]) * inv_l,
+                                                   __uint_as_float(r[8 * v + 2 * e + 1]) * inv_l);
+                            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(O) + orow * D + ch * 32);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
+                                                 __uint_as_float(r[4 * v + 2]) * inv_l,
+                                                 __uint_as_float(r[4 * v + 3]) * inv_l);
+                    }
+                }
+                if (LSE != nullptr && store) LSE[orow] = (m + __log2f(l)) * kLn2;
+            }
+        }
+        if (!ok) record_failure(abort_flag, status);
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+__global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar_storage;
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(&bar_storage);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // Nothing ever arrives on this barrier: the bounded wait must give up.
+    bool ok = mbar_wait_bounded(b, 0, reinterpret_cast<volatile int*>(&abort_flag), limit_ns);
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (!ok && threadIdx.x == 0) atomicExch(status, kDevStatusTimeout);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                      cudaStream_t st) {
+    using Cf = Cfg<D>;
+    auto kern = attn_bf16_tc_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((p.N + 2 * BM - 1) / (2 * BM)), (unsigned)(p.B * p.H));
+    const float c_log2 = p.scale * 1.4426950408889634f;
+    kern<<<grid, kThreads, Cf::kSmemBytes, st>>>(*tmQ, *tmK, *tmV, p.O, p.LSE, p.N, p.M, c_log2, p.out_bf16, p.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bf16_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                const CUtensorMap* tmV, int /*num_sms*/, cudaStream_t st) {
+    if (p.d == 64) return p.causal ? launch_tc<64, true>(p, tmQ, tmK, tmV, st) : launch_tc<64, false>(p, tmQ, tmK, tmV, st);
+    if (p.d == 128)
+        return p.causal ? launch_tc<128, true>(p, tmQ, tmK, tmV, st) : launch_tc<128, false>(p, tmQ, tmK, tmV, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_selftest_wait(int* status, uint64_t limit_ns, cudaStream_t st) {
+    selftest_wait_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,193 @@
+// fattn_api.cu -- the C ABI of libfattn (declared in include/fattn.h).
+//
+// Host side only: argument validation, TMA tensor-map encoding, kernel
+// dispatch on the caller's stream, and the per-device status word that the
+// kernels' bounded waits write on a timeout.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fattn.h"
+#include "fattn_internal.cuh"
+
+// Written by kernels whose bounded waits ran out; read and cleared by
+// fa_device_status().  One instance per device.
+__device__ int g_fa_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device address of g_fa_status on the current device (looked up once per device).
+int* status_word(int* err) {
+    static int* addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = FA_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) {
+            *err = FA_ERR_CUDA;
+            return nullptr;
+        }
+        addr[dev] = static_cast<int*>(p);
+    }
+    return addr[dev];
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [bh, rows, d] bf16 tensor -> 3-D tensor map, box 64 (d) x 128 (rows) x 1,
+// 128-byte swizzle, zero fill outside the tensor (ragged row tails).
+bool encode_bf16_3d(CUtensorMap* map, const void* ptr, long bh, long rows, int d) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool mul_fits(long a, long b, long limit) { return a > 0 && b > 0 && a <= limit / b; }
+
+int num_sms() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return FA_VERSION; }
+
+const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}
+
+int fa_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int M, int d,
+                float scale, int causal, int in_dtype, int out_dtype, void* stream) {
+    if (!Q || !K || !V || !O) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || N <= 0 || M <= 0 || d <= 0) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    const long kLim = 1L << 62;
+    const long bh = (long)B * H;
+    if (!mul_fits(bh, (long)(N > M ? N : M), kLim) || !mul_fits(bh * (N > M ? N : M), d, kLim / 4))
+        return FA_ERR_INVALID_ARG;
+    if (in_dtype != FA_F32 && in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    if (out_dtype != FA_F32 && out_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    if (bh > 65535) return FA_ERR_UNSUPPORTED;
+    if (in_dtype == FA_F32) {
+        if (out_dtype != FA_F32) return FA_ERR_UNSUPPORTED;
+        if (d != 16 && d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    } else {
+        if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    }
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (LSE && !aligned16(LSE)))
+        return FA_ERR_MISALIGNED;
+
+    int err = FA_OK;
+    int* status = status_word(&err);
+    if (status == nullptr) return err;
+    fa::AttnParams p{Q, K, V, O, LSE, B, H, N, M, d, scale, causal, out_dtype == FA_BF16 ? 1 : 0, status};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (in_dtype == FA_F32) {
+        e = fa::launch_attn_f32(p, st);
+    } else {
+        CUtensorMap tq, tk, tv;
+        if (!encode_bf16_3d(&tq, Q, bh, N, d) || !encode_bf16_3d(&tk, K, bh, M, d) ||
+            !encode_bf16_3d(&tv, V, bh, M, d))
+            return FA_ERR_CUDA;
+        e = fa::launch_attn_bf16_tc(p, &tq, &tk, &tv, num_sms(), st);
+    }
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, int in_dtype, int out_dtype,
+                    void* stream) {
+    if (!X || !P) return FA_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0 || !mul_fits(rows, cols, 1L << 60)) return FA_ERR_INVALID_ARG;
+    if ((in_dtype != FA_F32 && in_dtype != FA_BF16) || (out_dtype != FA_F32 && out_dtype != FA_BF16))
+        return FA_ERR_UNSUPPORTED;
+    if (!aligned16(X) || !aligned16(P) || (LSE && !aligned16(LSE))) return FA_ERR_MISALIGNED;
+    const cudaError_t e = fa::launch_softmax_rows(X, P, LSE, rows, cols, in_dtype == FA_BF16, out_dtype == FA_BF16,
+                                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_dtype, void* stream) {
+    if (!X || !LSE) return FA_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0 || !mul_fits(rows, cols, 1L << 60)) return FA_ERR_INVALID_ARG;
+    if (in_dtype != FA_F32 && in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(X) || !aligned16(LSE)) return FA_ERR_MISALIGNED;
+    const cudaError_t e =
+        fa::launch_logsumexp_rows(X, LSE, rows, cols, in_dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_device_status(void* stream, int reset) {
+    int err = FA_OK;
+    int* status = status_word(&err);
+    if (status == nullptr) return err;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+    if (reset && v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    return v == 0 ? FA_OK : v;
+}
+
+int fa_selftest_wait_timeout(int limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 1000000) return FA_ERR_INVALID_ARG;
+    int err = FA_OK;
+    int* status = status_word(&err);
+    if (status == nullptr) return err;
+    if (fa::launch_selftest_wait(status, (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return FA_ERR_CUDA;
+    return fa_device_status(stream, 1);
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// fattn_internal.cuh -- launchers shared between the C-ABI translation unit and
+// the kernel translation units.  Not part of the public interface.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Upper bound on any single in-kernel wait before the kernel gives up and
+// records a timeout (4 s of wall clock; a legitimate wait is microseconds).
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+// Status codes written into the per-device status word by kernels.
+constexpr int kDevStatusTimeout = 5;
+
+struct AttnParams {
+    const void* Q;
+    const void* K;
+    const void* V;
+    void* O;
+    float* LSE;        // may be null
+    int B, H, N, M, d;
+    float scale;       // > 0
+    int causal;
+    int out_bf16;      // 1: O is bf16, 0: O is fp32
+    int* status;       // device status word
+};
+
+// Row-wise kernels (softmax_rows.cu).
+cudaError_t launch_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, int in_bf16,
+                                int out_bf16, cudaStream_t stream);
+cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_bf16,
+                                  cudaStream_t stream);
+
+// fp32 CUDA-core attention (attn_f32.cu).  d in {16, 32, 64, 128}.
+cudaError_t launch_attn_f32(const AttnParams& p, cudaStream_t stream);
+
+// bf16 tensor-core attention (attn_tc.cu).  d in {64, 128}.  The three tensor
+// maps describe Q [B*H, N, d], K and V [B*H, M, d] as 3-D bf16 tensors with
+// a 64 x 128 box and 128-byte swizzle.
+cudaError_t launch_attn_bf16_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                const CUtensorMap* tmV, int num_sms, cudaStream_t stream);
+
+// One CTA waiting on an mbarrier that never completes (attn_tc.cu).
+cudaError_t launch_selftest_wait(int* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,155 @@
+"""Thin ctypes binding of libfattn (include/fattn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libfattn.so.  torch supplies device memory and the current stream.
+There is no CPU path: if the library is missing or no GPU is present, calls
+raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfattn.so")
+
+FA_F32, FA_BF16 = 0, 1
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT = range(6)
+
+# Every symbol include/fattn.h declares, with its ctypes signature.
+_c_int, _c_long, _c_float, _vp = ctypes.c_int, ctypes.c_long, ctypes.c_float, ctypes.c_void_p
+SIGNATURES = {
+    "fa_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
+                             _c_int, _c_int, _vp]),
+    "fa_softmax_rows": (_c_int, [_vp, _vp, _vp, _c_long, _c_long, _c_int, _c_int, _vp]),
+    "fa_logsumexp_rows": (_c_int, [_vp, _vp, _c_long, _c_long, _c_int, _vp]),
+    "fa_device_status": (_c_int, [_vp, _c_int]),
+    "fa_selftest_wait_timeout": (_c_int, [_c_int, _vp]),
+    "fa_status_string": (ctypes.c_char_p, [_c_int]),
+    "fa_version": (_c_int, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed: {status_string(status)} ({status})")
+
+
+def lib():
+    """Load libfattn.so (built in-tree by online_softmax_10_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libfattn.so is not built ({LIB_PATH}); run online_softmax_10_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype, f.argtypes = res, args
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return lib().fa_version()
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return FA_F32
+    if dt == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError("libfattn works on CUDA tensors only (no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def attn_fwd(q, k, v, scale: float | None = None, causal: bool = False, out_dtype=None, out=None, lse=None,
+             want_lse: bool = True, stream=None):
+    """O = softmax(scale * q k^T [+ causal]) v and LSE, through fa_attn_fwd.
+
+    q [B,H,N,d], k/v [B,H,M,d] contiguous CUDA tensors (bf16 or fp32).
+    Returns (o, lse); lse is None when want_lse is False and lse is None.
+    """
+    _check_cuda(q, k, v)
+    B, H, N, d = q.shape
+    M = k.shape[2]
+    if k.shape != (B, H, M, d) or v.shape != (B, H, M, d) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v shapes/dtypes do not match")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=out_dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_cuda(out, *([lse] if lse is not None else []))
+    rc = lib().fa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, M, d, float(scale),
+                           int(bool(causal)), _dtype_code(q.dtype), _dtype_code(out.dtype), _stream(stream))
+    if rc != FA_OK:
+        raise FattnError(rc, "fa_attn_fwd")
+    return out, lse
+
+
+def softmax_rows(x, out_dtype=None, out=None, lse=None, want_lse: bool = True, stream=None):
+    """Row-wise softmax of a 2-D CUDA tensor through fa_softmax_rows. Returns (p, lse)."""
+    _check_cuda(x)
+    rows, cols = x.shape
+    out_dtype = out_dtype or x.dtype
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype, device=x.device)
+    if lse is None and want_lse:
+        lse = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    rc = lib().fa_softmax_rows(_ptr(x), _ptr(out), _ptr(lse), rows, cols, _dtype_code(x.dtype),
+                               _dtype_code(out.dtype), _stream(stream))
+    if rc != FA_OK:
+        raise FattnError(rc, "fa_softmax_rows")
+    return out, lse
+
+
+def logsumexp_rows(x, out=None, stream=None):
+    """Row-wise log-sum-exp of a 2-D CUDA tensor through fa_logsumexp_rows."""
+    _check_cuda(x)
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    rc = lib().fa_logsumexp_rows(_ptr(x), _ptr(out), rows, cols, _dtype_code(x.dtype), _stream(stream))
+    if rc != FA_OK:
+        raise FattnError(rc, "fa_logsumexp_rows")
+    return out
+
+
+def device_status(reset: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the device status word (FA_OK or an error code)."""
+    return lib().fa_device_status(_stream(stream), int(bool(reset)))
+
+
+def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> int:
+    return lib().fa_selftest_wait_timeout(int(limit_us), _stream(stream))

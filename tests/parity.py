@@ -1,0 +1,58 @@
+"""Shared helpers of the GPU parity tests: run a case through the C ABI and
+compare with the oracle at the stated tolerances."""
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from online_softmax_10_gb300 import build as fbuild
+from online_softmax_10_gb300 import fattn, inputs
+
+# Tolerances (stated for the method; see the module docstrings of the tests)
+O_TOL_F32 = 1e-5      # max-abs on O, fp32 inputs
+O_TOL_BF16 = 1e-2     # max-abs on O, bf16 inputs, fp32 accumulation
+LSE_REL = 1e-3        # relative on LSE (gated as |dLSE| <= 1e-3 * max(1, |LSE|))
+P_TOL_BF16 = 4e-3     # max-abs on softmax probabilities stored as bf16 (about one bf16 ulp at 1)
+P_TOL_F32 = 1e-5      # max-abs on softmax probabilities stored as fp32
+
+
+def ensure_built():
+    fbuild.build()
+    fattn.lib()
+
+
+def lse_ok(lse_gpu, lse_ref):
+    lse_gpu = np.asarray(lse_gpu, dtype=np.float64)
+    d = np.abs(lse_gpu - lse_ref)
+    return bool(np.all(d <= LSE_REL * np.maximum(1.0, np.abs(lse_ref)))), float(np.max(d / np.maximum(np.abs(lse_ref), 1e-30)))
+
+
+def to_np(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def attn_case(q, k, v, causal, out_dtype=None, rows=None, stream=None):
+    """Run fa_attn_fwd on CPU tensors q, k, v (copied to the device) and the
+    oracle on the same bits.  Returns (max-abs O error, LSE ok, LSE max rel)."""
+    d = q.shape[-1]
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fattn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale, causal, out_dtype=out_dtype, stream=stream)
+    assert fattn.device_status(stream=stream) == fattn.FA_OK
+    o, lse = to_np(o), to_np(lse)
+    if rows is None:
+        O_ref, L_ref = oracle.attn_fwd(q, k, v, scale, causal)
+        O_g, L_g = o, lse
+    else:
+        rows = np.asarray(rows)
+        O_ref, L_ref = oracle.attn_fwd(q, k, v, scale, causal, rows=rows)
+        O_g = o.reshape(-1, d)[rows]
+        L_g = lse.reshape(-1)[rows]
+    assert np.all(np.isfinite(O_g)) and np.all(np.isfinite(L_g))
+    err = float(np.max(np.abs(O_g - O_ref)))
+    ok, rel = lse_ok(L_g, L_ref)
+    return err, ok, rel
+
+
+def workload_attn(w):
+    return inputs.workload_attn_inputs(w)
