@@ -352,6 +352,41 @@ def run_ours(args, world_size, rank, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def run_only(args):
+    """One kernel on one shape, for profiling captures (prints a short JSON
+    line that is not the benchmark's contract line)."""
+    import torch
+    from online_softmax_10_gb300 import build as fbuild
+    from online_softmax_10_gb300 import fattn, inputs
+    fbuild.build()
+    torch.cuda.set_device(0)
+    if args.only == "attn":
+        B, H, N, M, d, causal = (int(x) for x in args.shape.split(","))
+        dt = torch.float32 if args.f32 else torch.bfloat16
+        q, k, v = (t.cuda() for t in inputs.attn_inputs(B, H, N, M, d, dt, seed=3))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        fn = lambda: fattn.attn_fwd(q, k, v, 1.0 / math.sqrt(d), bool(causal), out=o, lse=lse)
+        work = 4.0 * B * H * N * M * d / (2 if causal else 1)
+        unit, scale = "TFLOP/s", 1e12
+    else:
+        rows, cols = (int(x) for x in args.shape.split(","))
+        x = inputs.rows_inputs(rows, cols, torch.bfloat16, seed=1).cuda()
+        lse = torch.empty(rows, dtype=torch.float32, device="cuda")
+        if args.only == "rows":
+            p = torch.empty_like(x)
+            fn = lambda: fattn.softmax_rows(x, out=p, lse=lse)
+            work = rows * cols * 4.0 + rows * 4
+        else:
+            fn = lambda: fattn.logsumexp_rows(x, out=lse)
+            work = rows * cols * 2.0 + rows * 4
+        unit, scale = "GB/s", 1e9
+    total, per = time_launches(fn, args.steps, args.warmup, 1)
+    assert fattn.device_status() == fattn.FA_OK
+    print(json.dumps({"only": args.only, "shape": args.shape, "launches": args.steps,
+                      "us_per_launch": per * 1e6, "value": work / per / scale, "unit": unit}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -364,9 +399,16 @@ def main():
                     help="ncu dram bytes per attention launch, if captured for the current kernel")
     ap.add_argument("--rows-traffic", type=float, default=None,
                     help="ncu dram bytes per row-softmax launch, if captured for the current kernel")
+    ap.add_argument("--only", choices=["attn", "rows", "lse"], default=None,
+                    help="time one kernel on --shape only (profiling aid; not the contract line)")
+    ap.add_argument("--shape", default=None, help="attn: B,H,N,M,d,causal   rows/lse: rows,cols")
+    ap.add_argument("--f32", action="store_true", help="with --only attn: fp32 inputs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.only:
+        run_only(args)
+        return
     world_size, rank, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, world_size, rank)

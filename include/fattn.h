@@ -91,7 +91,7 @@ int fa_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE
  *
  *   X    [rows, cols]  row-major, dtype in_dtype (FA_BF16 or FA_F32)
  *   P    [rows, cols]  row-major, dtype out_dtype (FA_BF16 or FA_F32), written;
- *                      must not be NULL (it may alias X when the dtypes match)
+ *                      must not be NULL and must not overlap X
  *   LSE  [rows]        fp32, written; may be NULL = skip
  * Errors: FA_ERR_INVALID_ARG for NULL X/P, rows <= 0, cols <= 0, or
  * rows*cols overflowing; FA_ERR_UNSUPPORTED for other dtypes;

@@ -150,8 +150,11 @@ int fa_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, in
     if ((in_dtype != FA_F32 && in_dtype != FA_BF16) || (out_dtype != FA_F32 && out_dtype != FA_BF16))
         return FA_ERR_UNSUPPORTED;
     if (!aligned16(X) || !aligned16(P) || (LSE && !aligned16(LSE))) return FA_ERR_MISALIGNED;
+    int err = FA_OK;
+    int* status = status_word(&err);
+    if (status == nullptr) return err;
     const cudaError_t e = fa::launch_softmax_rows(X, P, LSE, rows, cols, in_dtype == FA_BF16, out_dtype == FA_BF16,
-                                                  static_cast<cudaStream_t>(stream));
+                                                  status, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -160,8 +163,11 @@ int fa_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_dt
     if (rows <= 0 || cols <= 0 || !mul_fits(rows, cols, 1L << 60)) return FA_ERR_INVALID_ARG;
     if (in_dtype != FA_F32 && in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
     if (!aligned16(X) || !aligned16(LSE)) return FA_ERR_MISALIGNED;
-    const cudaError_t e =
-        fa::launch_logsumexp_rows(X, LSE, rows, cols, in_dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+    int err = FA_OK;
+    int* status = status_word(&err);
+    if (status == nullptr) return err;
+    const cudaError_t e = fa::launch_logsumexp_rows(X, LSE, rows, cols, in_dtype == FA_BF16, status,
+                                                    static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

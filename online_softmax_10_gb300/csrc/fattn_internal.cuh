@@ -29,8 +29,8 @@ struct AttnParams {
 
 // Row-wise kernels (softmax_rows.cu).
 cudaError_t launch_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, int in_bf16,
-                                int out_bf16, cudaStream_t stream);
-cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_bf16,
+                                int out_bf16, int* status, cudaStream_t stream);
+cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_bf16, int* status,
                                   cudaStream_t stream);
 
 // fp32 CUDA-core attention (attn_f32.cu).  d in {16, 32, 64, 128}.

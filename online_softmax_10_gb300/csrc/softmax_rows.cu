@@ -11,10 +11,19 @@
 // That form is associative, so per-thread partials merge through warp
 // shuffles and shared memory in any order.
 //
-// Resident kernel: one CTA per row, each thread holds its slice of the row in
-// registers (NV 16-byte vectors), so X is read from HBM exactly once and P is
-// written once.  Loads and stores are 128-bit and coalesced (consecutive
-// threads own consecutive 16-byte vectors).
+// Pipelined kernel (rows of 16-64 KB whose byte length is a multiple of 16):
+// persistent, one CTA per SM.  A producer warp streams whole rows into a ring
+// of shared-memory stages with bulk TMA copies (mbarrier-tracked), so several
+// rows are in flight per SM at all times; 16 consumer warps take a row from
+// shared memory into registers (128-bit loads), release the stage, compute
+// exp once per element relative to their own max, merge (m, s) across the
+// CTA and write P with 128-bit coalesced stores.  X is read from HBM once and
+// P written once.
+// Resident kernel (other row lengths up to 64K elements): one CTA per row,
+// each thread holds its slice of the row in registers (NV 16-byte vectors),
+// also one read and one write.
+// Exponents are formed as (x - m) * log2 e, the difference first, so large
+// logits keep their precision.
 // Streaming kernels: rows longer than the resident capacity are reduced with
 // the per-thread online update over 16-byte vectors (one read for LSE only,
 // two reads when P is also written).
@@ -162,17 +171,16 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_resident(const TIn* __re
             for (int i = 0; i < V; ++i) m = fmaxf(m, v[k][i]);
         float s = 0.f;
         if (m != -CUDART_INF_F) {
-            const float mc = m * kLog2e;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < NV; ++k)
 #pragma unroll
-                for (int i = 0; i < V; ++i) acc[i & 3] += ex2(fmaf(v[k][i], kLog2e, -mc));
+                for (int i = 0; i < V; ++i) acc[i & 3] += ex2((v[k][i] - m) * kLog2e);
             s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
         block_merge<THREADS>(m, s, sm_m, sm_s);
-        // p = exp(x - M) / S = 2^(x log2e - (M log2e + log2 S))
-        const float bias = fmaf(m, kLog2e, __log2f(s));
+        // p = exp(x - M) / S = 2^((x - M) log2e - log2 S)
+        const float l2s = __log2f(s);
         TOut* p = P + row * cols;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -180,7 +188,7 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_resident(const TIn* __re
             if (e0 < cols) {
                 float o[V];
 #pragma unroll
-                for (int i = 0; i < V; ++i) o[i] = ex2(fmaf(v[k][i], kLog2e, -bias));
+                for (int i = 0; i < V; ++i) o[i] = ex2(fmaf(v[k][i] - m, kLog2e, -l2s));
                 const int valid = (int)((cols - e0) < V ? (cols - e0) : V);
                 store_out<TOut, V>(p + e0, o, vec_ok && valid == V, valid);
             }
@@ -216,12 +224,11 @@ __device__ __forceinline__ void row_online_ms(const TIn* __restrict__ x, long co
             for (int i = 0; i < V; ++i) bm = fmaxf(bm, v[u][i]);
         if (bm == -CUDART_INF_F) continue;
         const float mn = fmaxf(m, bm);
-        const float mc = mn * kLog2e;
         float acc = 0.f;
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc += ex2(fmaf(v[u][i], kLog2e, -mc));
+            for (int i = 0; i < V; ++i) acc += ex2((v[u][i] - mn) * kLog2e);
         s = s * ex2((m - mn) * kLog2e) + acc;  // m = -inf on the first block: 2^-inf = 0
         m = mn;
     }
@@ -252,7 +259,7 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_stream(const TIn* __rest
         float m, s;
         row_online_ms<TIn, THREADS, U>(x, cols, vec_ok != 0, m, s);
         block_merge<THREADS>(m, s, sm_m, sm_s);
-        const float bias = fmaf(m, kLog2e, __log2f(s));
+        const float l2s = __log2f(s);
         TOut* p = P + row * cols;
         const long nvec = (cols + V - 1) / V;
         for (long vi = threadIdx.x; vi < nvec; vi += THREADS) {
@@ -265,11 +272,226 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_stream(const TIn* __rest
                 for (int i = 0; i < V; ++i) f[i] = i < valid ? Elem<TIn>::load1(x + e0 + i) : 0.f;
             }
 #pragma unroll
-            for (int i = 0; i < V; ++i) f[i] = ex2(fmaf(f[i], kLog2e, -bias));
+            for (int i = 0; i < V; ++i) f[i] = ex2(fmaf(f[i] - m, kLog2e, -l2s));
             store_out<TOut, V>(p + e0, f, vec_ok && valid == V, valid);
         }
         if (LSE != nullptr && threadIdx.x == 0) LSE[row] = m + logf(s);
     }
+}
+
+
+// ------------------------------------------------------------------ pipelined
+constexpr int kTmaConsumers = 512;                 // 16 consumer warps
+constexpr int kTmaThreads = kTmaConsumers + 32;    // + 1 producer warp
+constexpr int kTmaMaxStages = 4;
+constexpr uint32_t kTmaSmemBudget = 200 * 1024;
+constexpr uint32_t kTmaBarBytes = 128;             // full[4], empty[4], red
+constexpr uint32_t kTmaSmemExtra = 128 /* alignment */ + kTmaBarBytes + 2 * 16 * 8 /* (m, s) slots */ + 16;
+
+// One CTA per SM; rows r = blockIdx.x + i * gridDim.x go through a ring of
+// `nst` shared-memory stages of `stage_bytes` each.
+template <typename TIn, typename TOut, bool WRITE_P, int NV>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restrict__ LSE, long rows, long cols,
+                 uint32_t stage_bytes, int nst, int* status) {
+    constexpr int V = Elem<TIn>::kVec;
+    constexpr int W = kTmaConsumers / 32;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 127u) & ~127u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    // after the stages: mbarriers, then the (m, s) slots [2][W], then the abort flag
+    const uint32_t bar0 = base + (uint32_t)nst * stage_bytes;
+    float2* red = reinterpret_cast<float2*>(gbase + (uint32_t)nst * stage_bytes + kTmaBarBytes);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * W);
+    auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+    auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kTmaMaxStages + s); };
+    const uint32_t red_bar = bar0 + 8u * (uint32_t)(2 * kTmaMaxStages);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t row_bytes = (uint32_t)(cols * (long)sizeof(TIn));
+    const long nvec = cols / V;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), W);
+        }
+        mbar_init(red_bar, W);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == W) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();  // every row is read exactly once
+            long issued = 0;
+            for (long r = blockIdx.x; r < rows; r += gridDim.x, ++issued) {
+                const int s = (int)(issued % nst);
+                const uint32_t ph = (uint32_t)(issued / nst) & 1u;
+                if (!mbar_wait_bounded(empty(s), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                    *abort_flag = 1;
+                    atomicExch(status, kDevStatusTimeout);
+                    break;
+                }
+                mbar_expect_tx(full(s), row_bytes);
+                const char* src = reinterpret_cast<const char*>(X + r * cols);
+                const uint32_t dst = base + (uint32_t)s * stage_bytes;
+                for (uint32_t off = 0; off < row_bytes; off += 32768u) {
+                    const uint32_t n = row_bytes - off < 32768u ? row_bytes - off : 32768u;
+                    bulk_load(dst + off, src + off, n, full(s), pol);
+                }
+            }
+            // drain: the copies this thread issued have landed before it exits
+            for (long i = issued - nst < 0 ? 0 : issued - nst; i < issued; ++i)
+                mbar_wait_bounded(full((int)(i % nst)), (uint32_t)(i / nst) & 1u, nullptr, kWaitLimitNs);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumers
+    const float kc = kLog2e;
+    long i = 0;
+    for (long r = blockIdx.x; r < rows; r += gridDim.x, ++i) {
+        const int s = (int)(i % nst);
+        const uint32_t ph = (uint32_t)(i / nst) & 1u;
+        bool ok = mbar_wait_bounded(full(s), ph, abort_flag, kWaitLimitNs);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
+            *abort_flag = 1;
+            atomicExch(status, kDevStatusTimeout);
+            break;
+        }
+        // the row slice into registers, then the stage goes back to the producer
+        const TIn* srow = reinterpret_cast<const TIn*>(gbase + (uint32_t)s * stage_bytes);
+        float v[NV][V];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const long vi = threadIdx.x + (long)k * kTmaConsumers;
+            if (vi < nvec) {
+                const uint4 u = *reinterpret_cast<const uint4*>(srow + vi * V);
+                if constexpr (V == 8) {
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        v[k][2 * e] = __uint_as_float(w[e] << 16);
+                        v[k][2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+                    }
+                } else {
+                    v[k][0] = __uint_as_float(u.x); v[k][1] = __uint_as_float(u.y);
+                    v[k][2] = __uint_as_float(u.z); v[k][3] = __uint_as_float(u.w);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) v[k][e] = -CUDART_INF_F;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));
+        // this thread's (m, s); v becomes exp(v - m) in place
+        float m = -CUDART_INF_F;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < V; ++e) m = fmaxf(m, v[k][e]);
+        float sum = 0.f;
+        if (m != -CUDART_INF_F) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < NV; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const float ex = ex2((v[k][e] - m) * kc);
+                    if (WRITE_P) v[k][e] = ex;
+                    acc[e & 3] += ex;
+                }
+            sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        }
+        // merge (m, s): within the warp, then the 16 warps through shared memory
+        float M = m, S = sum;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xFFFFFFFFu, M, off);
+            const float s2 = __shfl_xor_sync(0xFFFFFFFFu, S, off);
+            merge_ms(M, S, m2, s2);
+        }
+        // (a bounded mbarrier exchange rather than a named barrier, so a warp
+        // that gave up can never leave the others waiting forever)
+        float2* slot = red + (i & 1) * W;
+        if (lane == 0) slot[warp] = make_float2(M, S);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(red_bar);
+        ok = mbar_wait_bounded(red_bar, (uint32_t)(i & 1), abort_flag, kWaitLimitNs);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
+            *abort_flag = 1;
+            atomicExch(status, kDevStatusTimeout);
+            break;
+        }
+        {
+            const float2 a = slot[lane & (W - 1)];
+            M = a.x;
+            S = a.y;
+#pragma unroll
+            for (int off = W / 2; off > 0; off >>= 1) {
+                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, M, off);
+                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, S, off);
+                merge_ms(M, S, m2, s2);
+            }
+        }
+        if (WRITE_P) {
+            // p = exp(x - m) * exp(m - M) / S
+            const float f = m == -CUDART_INF_F ? 0.f : ex2((m - M) * kc) / S;
+            TOut* prow = P + r * cols;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const long vi = threadIdx.x + (long)k * kTmaConsumers;
+                if (vi < nvec) {
+                    float o[V];
+#pragma unroll
+                    for (int e = 0; e < V; ++e) o[e] = v[k][e] * f;
+                    store_out<TOut, V>(prow + vi * V, o, true, V);
+                }
+            }
+        }
+        if (LSE != nullptr && threadIdx.x == 0) LSE[r] = M + logf(S);
+    }
+}
+
+int device_sms() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+// Launch the pipelined kernel if the row shape suits it; returns false if not.
+template <typename TIn, typename TOut, bool WRITE_P>
+bool try_launch_tma(const TIn* X, TOut* P, float* LSE, long rows, long cols, int* status, cudaStream_t st,
+                    cudaError_t* err) {
+    constexpr int V = Elem<TIn>::kVec;
+    const long row_bytes = cols * (long)sizeof(TIn);
+    if (cols % V != 0 || row_bytes < 16384 || row_bytes > 65536 || rows < 64) return false;
+    const long nvec = cols / V;
+    const uint32_t stage = (uint32_t)((row_bytes + 127) / 128 * 128);
+    int nst = (int)(kTmaSmemBudget / stage);
+    nst = nst > kTmaMaxStages ? kTmaMaxStages : nst;
+    const uint32_t smem = (uint32_t)nst * stage + kTmaSmemExtra;
+    const long grid = rows < device_sms() ? rows : device_sms();
+    auto launch = [&](auto kern) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) {
+            kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(X, P, LSE, rows, cols, stage, nst, status);
+            e = cudaGetLastError();
+        }
+        *err = e;
+    };
+    if (nvec <= 2L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 2>);
+    else if (nvec <= 4L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4>);
+    else launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8>);
+    return true;
 }
 
 long grid_for_rows(long rows) {
@@ -278,8 +500,11 @@ long grid_for_rows(long rows) {
 }
 
 template <typename TIn, typename TOut>
-cudaError_t softmax_dispatch(const TIn* X, TOut* P, float* LSE, long rows, long cols, cudaStream_t st) {
+cudaError_t softmax_dispatch(const TIn* X, TOut* P, float* LSE, long rows, long cols, int* status,
+                             cudaStream_t st) {
     constexpr int V = Elem<TIn>::kVec;
+    cudaError_t terr;
+    if (try_launch_tma<TIn, TOut, true>(X, P, LSE, rows, cols, status, st, &terr)) return terr;
     const int vec_ok = (cols % V) == 0;
     const long nvec = (cols + V - 1) / V;
     const dim3 grid((unsigned)grid_for_rows(rows));
@@ -299,8 +524,10 @@ cudaError_t softmax_dispatch(const TIn* X, TOut* P, float* LSE, long rows, long 
 }
 
 template <typename TIn>
-cudaError_t lse_dispatch(const TIn* X, float* LSE, long rows, long cols, cudaStream_t st) {
+cudaError_t lse_dispatch(const TIn* X, float* LSE, long rows, long cols, int* status, cudaStream_t st) {
     constexpr int V = Elem<TIn>::kVec;
+    cudaError_t terr;
+    if (try_launch_tma<TIn, float, false>(X, (float*)nullptr, LSE, rows, cols, status, st, &terr)) return terr;
     const int vec_ok = (cols % V) == 0;
     const long nvec = (cols + V - 1) / V;
     const dim3 grid((unsigned)grid_for_rows(rows));
@@ -313,20 +540,21 @@ cudaError_t lse_dispatch(const TIn* X, float* LSE, long rows, long cols, cudaStr
 }  // namespace
 
 cudaError_t launch_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, int in_bf16, int out_bf16,
-                                cudaStream_t st) {
+                                int* status, cudaStream_t st) {
     using bf = __nv_bfloat16;
     if (in_bf16 && out_bf16)
-        return softmax_dispatch((const bf*)X, (bf*)P, LSE, rows, cols, st);
+        return softmax_dispatch((const bf*)X, (bf*)P, LSE, rows, cols, status, st);
     if (in_bf16)
-        return softmax_dispatch((const bf*)X, (float*)P, LSE, rows, cols, st);
+        return softmax_dispatch((const bf*)X, (float*)P, LSE, rows, cols, status, st);
     if (out_bf16)
-        return softmax_dispatch((const float*)X, (bf*)P, LSE, rows, cols, st);
-    return softmax_dispatch((const float*)X, (float*)P, LSE, rows, cols, st);
+        return softmax_dispatch((const float*)X, (bf*)P, LSE, rows, cols, status, st);
+    return softmax_dispatch((const float*)X, (float*)P, LSE, rows, cols, status, st);
 }
 
-cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_bf16, cudaStream_t st) {
-    if (in_bf16) return lse_dispatch((const __nv_bfloat16*)X, LSE, rows, cols, st);
-    return lse_dispatch((const float*)X, LSE, rows, cols, st);
+cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_bf16, int* status,
+                                  cudaStream_t st) {
+    if (in_bf16) return lse_dispatch((const __nv_bfloat16*)X, LSE, rows, cols, status, st);
+    return lse_dispatch((const float*)X, LSE, rows, cols, status, st);
 }
 
 }  // namespace fa
