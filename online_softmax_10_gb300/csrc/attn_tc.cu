@@ -12,7 +12,13 @@
 // "Softmax与Flash-Attention" page attributes to FlashAttention-2), so o~
 // stays on chip for the whole pass.
 //
-// CTA organisation (one CTA per 256 query rows of one (batch, head)):
+// Grid: one CTA per 256 query rows of one (batch, head), numbered so that the
+// hardware's in-order dispatch is a longest-first list schedule within groups
+// of heads: all query blocks of G heads (longest causal blocks first) before
+// the next G heads.  The group keeps the K/V tiles the in-flight CTAs share
+// resident in L2, and longest-first keeps the causal tail short.
+//
+// CTA organisation:
 //   warps 0-3  softmax warpgroup for Q tile 0 (rows q0 .. q0+127), one row per thread
 //   warps 4-7  softmax warpgroup for Q tile 1 (rows q0+128 .. q0+255)
 //   warp  8    TMA producer: Q tiles once, then a ring of K and V tiles
@@ -102,7 +108,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, void* __restrict__ O, float* __restrict__ LSE,
-                    int N, int M, float c_log2, int out_bf16, int* status) {
+                    int N, int M, float c_log2, int out_bf16, int* status, int nqb, int BH, int G) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -114,8 +120,13 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const long bh = blockIdx.y;
-    const int qblk = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;  // longest first
+    // unit -> (head, query block): groups of G heads, longest block first
+    const int u = (int)blockIdx.x;
+    const int g0 = (u / (G * nqb)) * G;
+    const int gh = min(G, BH - g0);
+    const int r = u - g0 * nqb;
+    const long bh = g0 + r % gh;
+    const int qblk = nqb - 1 - r / gh;
     const int q0 = qblk * 2 * BM;
     const int n0 = kv_tiles_for<CAUSAL>(q0, 0, N, M);
     const int n1 = kv_tiles_for<CAUSAL>(q0, 1, N, M);
@@ -293,10 +304,16 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     if (key >= M || (CAUSAL && key > qi)) sv[c] = -CUDART_INF_F;
                 }
             }
-            float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+            // row max: three-input max over four independent chains
+            float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-            for (int c = 4; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
-            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c_log2;
+            for (int c = 0; c < 128; c += 8) {
+                mx[0] = max3f(mx[0], sv[c], sv[c + 1]);
+                mx[1] = max3f(mx[1], sv[c + 2], sv[c + 3]);
+                mx[2] = max3f(mx[2], sv[c + 4], sv[c + 5]);
+                mx[3] = max3f(mx[3], sv[c + 6], sv[c + 7]);
+            }
+            const float m_tile = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c_log2;
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -309,18 +326,22 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     rescale = true;
                 }
             }
-            // p = 2^(s * scale * log2e - m); P (bf16) overwrites S in tensor memory
+            // p = 2^(s * scale * log2e - m), two lanes per packed FMA; P (bf16)
+            // overwrites S in tensor memory
             const float neg_m = m == -CUDART_INF_F ? 0.f : -m;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            const float2 cc = make_float2(c_log2, c_log2), nm = make_float2(neg_m, neg_m);
+            float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = ex2(fmaf(sv[2 * c], c_log2, neg_m));
-                const float p1 = ex2(fmaf(sv[2 * c + 1], c_log2, neg_m));
-                ls[c & 3] += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
+                const float2 t2 = fma2(make_float2(sv[2 * c], sv[2 * c + 1]), cc, nm);
+                const float2 p2 = make_float2(ex2(t2.x), ex2(t2.y));
+                ls[c & 3] = add2(ls[c & 3], p2);
+                pk[c] = pack_bf16x2(p2.x, p2.y);
             }
-            l = fmaf(l, alpha, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+            const float2 lsum = add2(add2(ls[0], ls[1]), add2(ls[2], ls[3]));
+            l = fmaf(l, alpha, lsum.x + lsum.y);
             tmem_st_x64(tS, pk);
             // o~ <- alpha o~ when the reference max was raised.  The previous
             // P V of this tile has completed: it was issued before the Q K^T
@@ -406,24 +427,33 @@ __global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
 
 template <int D, bool CAUSAL>
 cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                      cudaStream_t st) {
+                      int num_sms, cudaStream_t st) {
     using Cf = Cfg<D>;
     auto kern = attn_bf16_tc_kernel<D, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((p.N + 2 * BM - 1) / (2 * BM)), (unsigned)(p.B * p.H));
+    const int nqb = (p.N + 2 * BM - 1) / (2 * BM);
+    const int BH = p.B * p.H;
+    // heads per group: enough query blocks to keep every SM busy about twice over
+    int G = (2 * num_sms + nqb - 1) / nqb;
+    G = G < 1 ? 1 : (G > BH ? BH : G);
+    const dim3 grid((unsigned)((long)nqb * BH));
     const float c_log2 = p.scale * 1.4426950408889634f;
-    kern<<<grid, kThreads, Cf::kSmemBytes, st>>>(*tmQ, *tmK, *tmV, p.O, p.LSE, p.N, p.M, c_log2, p.out_bf16, p.status);
+    kern<<<grid, kThreads, Cf::kSmemBytes, st>>>(*tmQ, *tmK, *tmV, p.O, p.LSE, p.N, p.M, c_log2, p.out_bf16, p.status,
+                                                 nqb, BH, G);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bf16_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                                const CUtensorMap* tmV, int /*num_sms*/, cudaStream_t st) {
-    if (p.d == 64) return p.causal ? launch_tc<64, true>(p, tmQ, tmK, tmV, st) : launch_tc<64, false>(p, tmQ, tmK, tmV, st);
+                                const CUtensorMap* tmV, int num_sms, cudaStream_t st) {
+    if (p.d == 64)
+        return p.causal ? launch_tc<64, true>(p, tmQ, tmK, tmV, num_sms, st)
+                        : launch_tc<64, false>(p, tmQ, tmK, tmV, num_sms, st);
     if (p.d == 128)
-        return p.causal ? launch_tc<128, true>(p, tmQ, tmK, tmV, st) : launch_tc<128, false>(p, tmQ, tmK, tmV, st);
+        return p.causal ? launch_tc<128, true>(p, tmQ, tmK, tmV, num_sms, st)
+                        : launch_tc<128, false>(p, tmQ, tmK, tmV, num_sms, st);
     return cudaErrorInvalidValue;
 }
 
