@@ -132,6 +132,13 @@ int fa_device_status(void* stream, int reset);
  */
 int fa_selftest_wait_timeout(int limit_us, void* stream);
 
+/*
+ * fa_last_cuda_error -- the CUDA runtime's message for the error behind the
+ * most recent FA_ERR_CUDA returned on the calling thread ("no error" if none).
+ * Static storage, never NULL.  (No counterpart on the pages.)
+ */
+const char* fa_last_cuda_error(void);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* fa_status_string(int status);
 

@@ -23,20 +23,32 @@ constexpr int kMaxDevices = 64;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+// FA_OK, or FA_ERR_CUDA with the runtime error remembered for fa_last_cuda_error().
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return FA_OK;
+    t_last_cuda_error = e;
+    return FA_ERR_CUDA;
+}
+
 // Device address of g_fa_status on the current device (looked up once per device).
 int* status_word(int* err) {
     static int* addr[kMaxDevices] = {};
     static std::mutex mu;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        *err = FA_ERR_CUDA;
+    const cudaError_t ge = cudaGetDevice(&dev);
+    if (ge != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = cuda_status(ge == cudaSuccess ? cudaErrorInvalidDevice : ge);
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(mu);
     if (addr[dev] == nullptr) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) {
-            *err = FA_ERR_CUDA;
+        const cudaError_t se = cudaGetSymbolAddress(&p, g_fa_status);
+        if (se != cudaSuccess) {
+            *err = cuda_status(se);
             return nullptr;
         }
         addr[dev] = static_cast<int*>(p);
@@ -91,6 +103,8 @@ extern "C" {
 
 int fa_version(void) { return FA_VERSION; }
 
+const char* fa_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda_error); }
+
 const char* fa_status_string(int status) {
     switch (status) {
         case FA_OK: return "FA_OK";
@@ -140,7 +154,7 @@ int fa_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE
             return FA_ERR_CUDA;
         e = fa::launch_attn_bf16_tc(p, &tq, &tk, &tv, num_sms(), st);
     }
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return cuda_status(e);
 }
 
 int fa_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, int in_dtype, int out_dtype,
@@ -155,7 +169,7 @@ int fa_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, in
     if (status == nullptr) return err;
     const cudaError_t e = fa::launch_softmax_rows(X, P, LSE, rows, cols, in_dtype == FA_BF16, out_dtype == FA_BF16,
                                                   status, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return cuda_status(e);
 }
 
 int fa_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_dtype, void* stream) {
@@ -168,19 +182,22 @@ int fa_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_dt
     if (status == nullptr) return err;
     const cudaError_t e = fa::launch_logsumexp_rows(X, LSE, rows, cols, in_dtype == FA_BF16, status,
                                                     static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return cuda_status(e);
 }
 
 int fa_device_status(void* stream, int reset) {
     int err = FA_OK;
     int* status = status_word(&err);
     if (status == nullptr) return err;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
     int v = 0;
-    if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+    e = cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
     if (reset && v != 0) {
         const int zero = 0;
-        if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+        e = cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_status(e);
     }
     return v == 0 ? FA_OK : v;
 }
@@ -190,9 +207,8 @@ int fa_selftest_wait_timeout(int limit_us, void* stream) {
     int err = FA_OK;
     int* status = status_word(&err);
     if (status == nullptr) return err;
-    if (fa::launch_selftest_wait(status, (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream)) !=
-        cudaSuccess)
-        return FA_ERR_CUDA;
+    const cudaError_t e = fa::launch_selftest_wait(status, (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
     return fa_device_status(stream, 1);
 }
 

@@ -460,6 +460,185 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
     }
 }
 
+
+// LSE only, pipelined: the same producer as softmax_rows_tma, but two groups
+// of 8 consumer warps take alternate rows, so that one group's merge latency
+// overlaps the other's arithmetic.  The stage count is even, so stage s only
+// ever holds rows of group s % 2 and each group consumes its stages' phases in
+// order (a group can never run a phase ahead on a stage the other group still
+// owns).  A group copies its row slice into registers (packed), releases the
+// stage, then folds the values into a running (m, s) four vectors at a time
+// (the online normaliser applied per chunk).
+constexpr int kLseGroups = 2;
+constexpr int kLseGroupThreads = kTmaConsumers / kLseGroups;  // 256
+
+template <typename TIn, int NV>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows, long cols, uint32_t stage_bytes,
+                   int nst, int* status) {
+    constexpr int V = Elem<TIn>::kVec;
+    constexpr int WG = kLseGroupThreads / 32;  // warps per group
+    constexpr int CH = 4;                      // vectors per online step
+    static_assert(NV % (2 * CH) == 0, "NV must be a multiple of two chunks");
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 127u) & ~127u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    // after the stages: full[4], empty[4], red[2]; then (m, s) slots [group][2][WG]; then the abort flag
+    const uint32_t bar0 = base + (uint32_t)nst * stage_bytes;
+    float2* red = reinterpret_cast<float2*>(gbase + (uint32_t)nst * stage_bytes + kTmaBarBytes);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kLseGroups * 2 * WG);
+    auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+    auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kTmaMaxStages + s); };
+    auto red_bar = [&](int g) { return bar0 + 8u * (uint32_t)(2 * kTmaMaxStages + g); };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t row_bytes = (uint32_t)(cols * (long)sizeof(TIn));
+    const long nvec = cols / V;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), WG);  // released by the group that owns the stage
+        }
+        for (int g = 0; g < kLseGroups; ++g) mbar_init(red_bar(g), WG);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kTmaConsumers / 32) {
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            long issued = 0;
+            for (long r = blockIdx.x; r < rows; r += gridDim.x, ++issued) {
+                const int s = (int)(issued % nst);
+                const uint32_t ph = (uint32_t)(issued / nst) & 1u;
+                if (!mbar_wait_bounded(empty(s), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                    *abort_flag = 1;
+                    atomicExch(status, kDevStatusTimeout);
+                    break;
+                }
+                mbar_expect_tx(full(s), row_bytes);
+                const char* src = reinterpret_cast<const char*>(X + r * cols);
+                const uint32_t dst = base + (uint32_t)s * stage_bytes;
+                for (uint32_t off = 0; off < row_bytes; off += 32768u) {
+                    const uint32_t n = row_bytes - off < 32768u ? row_bytes - off : 32768u;
+                    bulk_load(dst + off, src + off, n, full(s), pol);
+                }
+            }
+            for (long i = issued - nst < 0 ? 0 : issued - nst; i < issued; ++i)
+                mbar_wait_bounded(full((int)(i % nst)), (uint32_t)(i / nst) & 1u, nullptr, kWaitLimitNs);
+        }
+        return;
+    }
+
+    const int g = warp / WG;                        // consumer group
+    const int gw = warp % WG;                       // warp within the group
+    const int gt = threadIdx.x % kLseGroupThreads;  // thread within the group
+    const float2 cc = make_float2(kLog2e, kLog2e);
+    long k = 0;                                     // rows this group has done
+    for (long i = g; blockIdx.x + i * (long)gridDim.x < rows; i += kLseGroups, ++k) {
+        const long r = blockIdx.x + i * (long)gridDim.x;
+        const int s = (int)(i % nst);
+        const uint32_t ph = (uint32_t)(i / nst) & 1u;
+        bool ok = mbar_wait_bounded(full(s), ph, abort_flag, kWaitLimitNs);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
+            *abort_flag = 1;
+            atomicExch(status, kDevStatusTimeout);
+            break;
+        }
+        // this thread's slice in two halves, still packed; the stage goes back
+        // to the producer as soon as the second half is in registers
+        const TIn* srow = reinterpret_cast<const TIn*>(gbase + (uint32_t)s * stage_bytes);
+        constexpr int NH = NV / 2;
+        float m = -CUDART_INF_F, sum = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint4 raw[NH];
+#pragma unroll
+            for (int kk = 0; kk < NH; ++kk) {
+                const long vi = gt + (long)(half * NH + kk) * kLseGroupThreads;
+                raw[kk] = vi < nvec ? *reinterpret_cast<const uint4*>(srow + vi * V) : make_uint4(0, 0, 0, 0);
+            }
+            if (half == 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty(s));
+            }
+#pragma unroll
+            for (int k0 = 0; k0 < NH; k0 += CH) {
+                float v[CH][V];
+#pragma unroll
+                for (int kk = 0; kk < CH; ++kk) {
+                    const bool in = gt + (long)(half * NH + k0 + kk) * kLseGroupThreads < nvec;
+                    const uint4 u = raw[k0 + kk];
+                    if constexpr (V == 8) {
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            v[kk][2 * e] = in ? __uint_as_float(w[e] << 16) : -CUDART_INF_F;
+                            v[kk][2 * e + 1] = in ? __uint_as_float(w[e] & 0xFFFF0000u) : -CUDART_INF_F;
+                        }
+                    } else {
+                        v[kk][0] = in ? __uint_as_float(u.x) : -CUDART_INF_F;
+                        v[kk][1] = in ? __uint_as_float(u.y) : -CUDART_INF_F;
+                        v[kk][2] = in ? __uint_as_float(u.z) : -CUDART_INF_F;
+                        v[kk][3] = in ? __uint_as_float(u.w) : -CUDART_INF_F;
+                    }
+                }
+                float cm = -CUDART_INF_F;
+#pragma unroll
+                for (int kk = 0; kk < CH; ++kk)
+#pragma unroll
+                    for (int e = 0; e < V; e += 2) cm = max3f(cm, v[kk][e], v[kk][e + 1]);
+                if (cm == -CUDART_INF_F) continue;
+                const float mn = fmaxf(m, cm);
+                // only the sum is kept, so the exponent is one packed FMA:
+                // x log2e - mn log2e (enough precision for log-sum-exp)
+                const float2 nmc = make_float2(-mn * kLog2e, -mn * kLog2e);
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int kk = 0; kk < CH; ++kk)
+#pragma unroll
+                    for (int e = 0; e < V; e += 2) {
+                        const float2 t2 = fma2(make_float2(v[kk][e], v[kk][e + 1]), cc, nmc);
+                        acc = add2(acc, make_float2(ex2(t2.x), ex2(t2.y)));
+                    }
+                sum = sum * ex2((m - mn) * kLog2e) + (acc.x + acc.y);
+                m = mn;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+            const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+            merge_ms(m, sum, m2, s2);
+        }
+        float2* slot = red + (g * 2 + (k & 1)) * WG;
+        if (lane == 0) slot[gw] = make_float2(m, sum);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(red_bar(g));
+        ok = mbar_wait_bounded(red_bar(g), (uint32_t)(k & 1), abort_flag, kWaitLimitNs);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
+            *abort_flag = 1;
+            atomicExch(status, kDevStatusTimeout);
+            break;
+        }
+        if (gw == 0) {
+            const float2 a = slot[lane & (WG - 1)];
+            float M = a.x, S = a.y;
+#pragma unroll
+            for (int off = WG / 2; off > 0; off >>= 1) {
+                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, M, off);
+                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, S, off);
+                merge_ms(M, S, m2, s2);
+            }
+            if (lane == 0) LSE[r] = M + logf(S);
+        }
+    }
+}
+
 int device_sms() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -491,6 +670,34 @@ bool try_launch_tma(const TIn* X, TOut* P, float* LSE, long rows, long cols, int
     if (nvec <= 2L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 2>);
     else if (nvec <= 4L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4>);
     else launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8>);
+    return true;
+}
+
+
+// Launch the pipelined LSE-only kernel if the row shape suits it.
+template <typename TIn>
+bool try_launch_lse_tma(const TIn* X, float* LSE, long rows, long cols, int* status, cudaStream_t st,
+                        cudaError_t* err) {
+    constexpr int V = Elem<TIn>::kVec;
+    const long row_bytes = cols * (long)sizeof(TIn);
+    if (cols % V != 0 || row_bytes < 16384 || row_bytes > 65536 || rows < 64) return false;
+    const long nvec = cols / V;
+    const uint32_t stage = (uint32_t)((row_bytes + 127) / 128 * 128);
+    int nst = (int)(kTmaSmemBudget / stage);
+    nst = nst > kTmaMaxStages ? kTmaMaxStages : nst;
+    nst &= ~1;  // even: stage s belongs to consumer group s % 2
+    const uint32_t smem = (uint32_t)nst * stage + kTmaSmemExtra;
+    const long grid = rows < device_sms() ? rows : device_sms();
+    auto launch = [&](auto kern) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) {
+            kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(X, LSE, rows, cols, stage, nst, status);
+            e = cudaGetLastError();
+        }
+        *err = e;
+    };
+    if (nvec <= 8L * kLseGroupThreads) launch(logsumexp_rows_tma<TIn, 8>);
+    else launch(logsumexp_rows_tma<TIn, 16>);
     return true;
 }
 
@@ -527,7 +734,7 @@ template <typename TIn>
 cudaError_t lse_dispatch(const TIn* X, float* LSE, long rows, long cols, int* status, cudaStream_t st) {
     constexpr int V = Elem<TIn>::kVec;
     cudaError_t terr;
-    if (try_launch_tma<TIn, float, false>(X, (float*)nullptr, LSE, rows, cols, status, st, &terr)) return terr;
+    if (try_launch_lse_tma<TIn>(X, LSE, rows, cols, status, st, &terr)) return terr;
     const int vec_ok = (cols % V) == 0;
     const long nvec = (cols + V - 1) / V;
     const dim3 grid((unsigned)grid_for_rows(rows));

@@ -30,6 +30,7 @@ SIGNATURES = {
     "fa_device_status": (_c_int, [_vp, _c_int]),
     "fa_selftest_wait_timeout": (_c_int, [_c_int, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),
+    "fa_last_cuda_error": (ctypes.c_char_p, []),
     "fa_version": (_c_int, []),
 }
 
@@ -40,7 +41,8 @@ _lib = None
 class FattnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what} failed: {status_string(status)} ({status})")
+        detail = f": {lib().fa_last_cuda_error().decode()}" if status == FA_ERR_CUDA else ""
+        super().__init__(f"{what} failed: {status_string(status)} ({status}){detail}")
 
 
 def lib():
