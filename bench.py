@@ -328,6 +328,20 @@ def run_ours(args, world_size, rank, local_rank):
     l_bytes = rw.rows * rw.cols * 2 + rw.rows * 4
     del x, p
 
+    # ---- split-KV on a decode-like shape (few query rows, long keys): the
+    # (head, query block) units alone cover 8 of the SMs
+    sq, sk, sv = (t.cuda() for t in inputs.attn_inputs(1, 8, 256, 65536, 128, torch.bfloat16, seed=6))
+    s_flops = 4.0 * 8 * 256 * 65536 * 128
+    nsplit = fattn.splitkv_num_splits(1, 8, 256, 65536, 128, False)
+    ws = torch.empty(max(1, fattn.splitkv_workspace_bytes(1, 8, 256, 128, nsplit)), dtype=torch.uint8, device="cuda")
+    so = torch.empty_like(sq)
+    sl = torch.empty((1, 8, 256), dtype=torch.float32, device="cuda")
+    _, s_per = time_launches(lambda: fattn.attn_fwd_splitkv(sq, sk, sv, 128 ** -0.5, False, num_splits=nsplit,
+                                                           workspace=ws, out=so, lse=sl), 50, 5, world_size)
+    _, u_per = time_launches(lambda: fattn.attn_fwd(sq, sk, sv, 128 ** -0.5, False, out=so, lse=sl), 20, 3,
+                             world_size)
+    del sq, sk, sv, ws
+
     # ---- fp32 attention workload (N = M = 64, d = 64): launch-latency bound
     fw = inputs.ATTN_F32_64
     fq, fk, fv = (t.cuda() for t in inputs.workload_attn_inputs(fw))
@@ -368,6 +382,9 @@ def run_ours(args, world_size, rank, local_rank):
                         "launches": rsteps, "l2": "input 268 MB > 129 MB L2, no flush"},
         "logsumexp_rows": {"workload": rw.name, "value": l_bytes / l_per / 1e9, "unit": "GB/s",
                            "us_per_launch": l_per * 1e6, "frac": l_bytes / l_per / 1e9 / peaks["hbm_gbs"]},
+        "attn_splitkv": {"workload": "attn_bf16_B1_H8_N256_M65536_d128 (decode-like)", "splits": nsplit,
+                         "value": s_flops / s_per / 1e12, "unit": "TFLOP/s", "us_per_launch": s_per * 1e6,
+                         "unsplit_value": s_flops / u_per / 1e12},
         "attn_f32": {"workload": fw.name, "us_per_launch": f_per * 1e6,
                      "value": fw.flops() / f_per / 1e12, "unit": "TFLOP/s"},
     }

@@ -80,6 +80,44 @@ int fa_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE
                 int in_dtype, int out_dtype, void* stream);
 
 /*
+ * fa_attn_fwd_splitkv -- fa_attn_fwd with the key tiles of each 256-row query
+ * block split over `num_splits` CTAs, for shapes with too few (batch, head,
+ * query block) units to fill the GPU (few heads, short query, long keys).
+ * Split s returns a normalised partial output o_s and its log-sum-exp LSE_s;
+ * a second kernel merges them:
+ *     LSE = log sum_s e^{LSE_s},   O = sum_s e^{LSE_s - LSE} o_s,
+ * the merge of normalised block results of "从原始Softmax到在线Softmax",
+ * section on the block-wise online softmax (l_s = e^{LSE_s}).
+ *
+ *   Q, K, V, O, LSE, B, H, N, M, d, scale, causal, in_dtype, out_dtype:
+ *       as fa_attn_fwd; splitting (num_splits > 1) needs in_dtype FA_BF16.
+ *   num_splits  1..64, or 0 = fa_attn_splitkv_num_splits(); 1 is fa_attn_fwd.
+ *   workspace   caller-owned device scratch of at least
+ *               fa_attn_splitkv_workspace_bytes(B, H, N, d, S) bytes, 256-byte
+ *               aligned (fp32 partials [S][B*H][N][d], then fp32 LSE_s
+ *               [S][B*H][N]); not needed (may be NULL) when S = 1.  Its
+ *               contents are overwritten; calls sharing one workspace must not
+ *               overlap on the GPU.
+ * Errors: as fa_attn_fwd, plus FA_ERR_INVALID_ARG for num_splits outside
+ * 0..64 or a missing/too small workspace, FA_ERR_MISALIGNED for a workspace
+ * not 256-byte aligned, FA_ERR_UNSUPPORTED for fp32 inputs with S > 1.
+ */
+int fa_attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                        int B, int H, int N, int M, int d, float scale, int causal,
+                        int num_splits, void* workspace, long workspace_bytes,
+                        int in_dtype, int out_dtype, void* stream);
+
+/* The split count fa_attn_fwd_splitkv uses for num_splits = 0 on the current
+ * device: 1 when the (batch, head, query block) units already fill it,
+ * otherwise enough splits to cover every SM, at most 64 and at least two key
+ * tiles per split.  (No counterpart on the pages.) */
+int fa_attn_splitkv_num_splits(int B, int H, int N, int M, int d, int causal);
+
+/* Workspace bytes fa_attn_fwd_splitkv needs for num_splits (1..64) splits;
+ * 0 for one split, -1 for invalid arguments.  (No counterpart on the pages.) */
+long fa_attn_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
+
+/*
  * fa_softmax_rows -- P[r, :] = softmax(X[r, :]) and LSE[r] = log sum_c exp X[r, c]
  * for every row, reading X from memory once when a row fits on chip
  * (cols <= 65536 for bf16, <= 32768 for fp32) and twice otherwise.

@@ -5,5 +5,6 @@ The compute path is the C-ABI library ``libfattn.so`` (include/fattn.h), built
 in-tree by :mod:`online_softmax_10_gb300.build`; :mod:`.fattn` is its thin
 binding.  :mod:`.inputs` holds the seeded synthetic input generators.
 """
-from .fattn import (FattnError, attn_fwd, device_status, logsumexp_rows, selftest_wait_timeout,  # noqa: F401
-                    softmax_rows, status_string, version)
+from .fattn import (FattnError, attn_fwd, attn_fwd_splitkv, device_status, logsumexp_rows,  # noqa: F401
+                    selftest_wait_timeout, softmax_rows, splitkv_num_splits, splitkv_workspace_bytes,
+                    status_string, version)

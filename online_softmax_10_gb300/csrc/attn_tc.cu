@@ -108,7 +108,8 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, void* __restrict__ O, float* __restrict__ LSE,
-                    int N, int M, float c_log2, int out_bf16, int* status, int nqb, int BH, int G) {
+                    int N, int M, float c_log2, int out_bf16, int* status, int nqb, int BH, int G, int S,
+                    float* __restrict__ Opart, float* __restrict__ Lpart) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -120,17 +121,27 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // unit -> (head, query block): groups of G heads, longest block first
-    const int u = (int)blockIdx.x;
+    // unit -> (head, query block, key split): groups of G heads, longest block
+    // first, the S splits of a block adjacent
+    const int split = (int)(blockIdx.x % (unsigned)S);
+    const int u = (int)(blockIdx.x / (unsigned)S);
     const int g0 = (u / (G * nqb)) * G;
     const int gh = min(G, BH - g0);
     const int r = u - g0 * nqb;
     const long bh = g0 + r % gh;
     const int qblk = nqb - 1 - r / gh;
     const int q0 = qblk * 2 * BM;
-    const int n0 = kv_tiles_for<CAUSAL>(q0, 0, N, M);
-    const int n1 = kv_tiles_for<CAUSAL>(q0, 1, N, M);
-    const int nk = max(n0, n1);
+    // This CTA covers key tiles [jb, jb + nk) of the ones its query block
+    // needs (all of them when S = 1); n0, n1 count the tiles of that range each
+    // Q tile uses, and j below runs over the range (key tile jb + j).
+    const int f0 = kv_tiles_for<CAUSAL>(q0, 0, N, M);
+    const int f1 = kv_tiles_for<CAUSAL>(q0, 1, N, M);
+    const int fk = max(f0, f1);
+    const int jb = (int)((long)split * fk / S);
+    const int je = (int)((long)(split + 1) * fk / S);
+    const int n0 = max(0, min(f0, je) - jb);
+    const int n1 = max(0, min(f1, je) - jb);
+    const int nk = je - jb;
 
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
@@ -178,7 +189,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 mbar_expect_tx(bar(C::KF(s)), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
                     tma_load_3d(base + C::kK + s * C::kTileBytes + a * kAtomBytes, &tmK, bar(C::KF(s)),
-                                a * 64, j * BN, (int)bh);
+                                a * 64, (jb + j) * BN, (int)bh);
                 issued_k = j + 1;
                 if (!mbar_wait_bounded(bar(C::VE(s)), ph ^ 1u, abort_flag, kWaitLimitNs)) {
                     record_failure(abort_flag, status);
@@ -187,7 +198,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 mbar_expect_tx(bar(C::VF(s)), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
                     tma_load_3d(base + C::kV + s * C::kTileBytes + a * kAtomBytes, &tmV, bar(C::VF(s)),
-                                a * 64, j * BN, (int)bh);
+                                a * 64, (jb + j) * BN, (int)bh);
                 issued_v = j + 1;
             }
             // Drain: the last copy issued into each stage has landed before the
@@ -228,8 +239,9 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             bool ok = true;
             for (int t = 0; t < 2 && ok; ++t)
                 if (nt[t] > 0) ok = mbar_wait_bounded(bar(C::QF(t)), 0, abort_flag, kWaitLimitNs);
-            if (ok) ok = mbar_wait_bounded(bar(C::KF(0)), 0, abort_flag, kWaitLimitNs);
-            if (ok) {
+            // (a split may hold no key tile at all: then nothing is issued)
+            if (ok && nk > 0) ok = mbar_wait_bounded(bar(C::KF(0)), 0, abort_flag, kWaitLimitNs);
+            if (ok && nk > 0) {
                 tc_fence_after();
                 for (int t = 0; t < 2; ++t) {
                     if (nt[t] == 0) continue;
@@ -295,7 +307,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             float sv[128];
 #pragma unroll
             for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
-            const int k0 = j * BN;
+            const int k0 = (jb + j) * BN;
             const bool need_mask = (k0 + BN > M) || (CAUSAL && k0 + BN - 1 > q0 + t * BM);
             if (need_mask) {
 #pragma unroll
@@ -361,20 +373,32 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_arrive(bar(C::PF(t)));
         }
         // ------------------------------------------------------ epilogue
+        const long orow = bh * (long)N + qi;
+        const bool store = qi < N;
+        if (S > 1 && n == 0 && ok && store) {
+            // no key of this split is kept for this row: an empty partial
+            Lpart[(long)split * BH * N + orow] = -CUDART_INF_F;
+        }
         if (n > 0 && ok) {
             ok = mbar_wait_bounded(bar(C::OD(t)), 0, abort_flag, kWaitLimitNs);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (ok) {
                 tc_fence_after();
                 const float inv_l = 1.f / l;
-                const bool store = qi < N;
-                const long orow = bh * (long)N + qi;
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t r[32];
                     tmem_ld_x32(tO + ch * 32, r);
                     if (!store) continue;
-                    if (out_bf16) {
+                    if (S > 1) {
+                        // normalised partial o_s = o~_s / l_s, fp32
+                        float4* dst = reinterpret_cast<float4*>(Opart + ((long)split * BH * N + orow) * D + ch * 32);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
+                                                 __uint_as_float(r[4 * v + 2]) * inv_l,
+                                                 __uint_as_float(r[4 * v + 3]) * inv_l);
+                    } else if (out_bf16) {
                         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(O) + orow * D + ch * 32);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
@@ -394,7 +418,11 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                                                  __uint_as_float(r[4 * v + 3]) * inv_l);
                     }
                 }
-                if (LSE != nullptr && store) LSE[orow] = (m + __log2f(l)) * kLn2;
+                if (store) {
+                    const float lse = (m + __log2f(l)) * kLn2;
+                    if (S > 1) Lpart[(long)split * BH * N + orow] = lse;
+                    else if (LSE != nullptr) LSE[orow] = lse;
+                }
             }
         }
         if (!ok) record_failure(abort_flag, status);
@@ -437,10 +465,11 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtenso
     // heads per group: enough query blocks to keep every SM busy about twice over
     int G = (2 * num_sms + nqb - 1) / nqb;
     G = G < 1 ? 1 : (G > BH ? BH : G);
-    const dim3 grid((unsigned)((long)nqb * BH));
+    const int S = p.num_splits > 1 ? p.num_splits : 1;
+    const dim3 grid((unsigned)((long)nqb * BH * S));
     const float c_log2 = p.scale * 1.4426950408889634f;
     kern<<<grid, kThreads, Cf::kSmemBytes, st>>>(*tmQ, *tmK, *tmV, p.O, p.LSE, p.N, p.M, c_log2, p.out_bf16, p.status,
-                                                 nqb, BH, G);
+                                                 nqb, BH, G, S, p.Opart, p.Lpart);
     return cudaGetLastError();
 }
 

@@ -97,6 +97,54 @@ int num_sms() {
     return n;
 }
 
+
+// Argument checks shared by the attention entry points (nothing is enqueued).
+int check_attn_args(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int M,
+                    int d, float scale, int causal, int in_dtype, int out_dtype) {
+    if (!Q || !K || !V || !O) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || N <= 0 || M <= 0 || d <= 0) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    const long kLim = 1L << 62;
+    const long bh = (long)B * H;
+    if (!mul_fits(bh, (long)(N > M ? N : M), kLim) || !mul_fits(bh * (N > M ? N : M), d, kLim / 4))
+        return FA_ERR_INVALID_ARG;
+    if (in_dtype != FA_F32 && in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    if (out_dtype != FA_F32 && out_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    if (bh > 65535) return FA_ERR_UNSUPPORTED;
+    if (in_dtype == FA_F32) {
+        if (out_dtype != FA_F32) return FA_ERR_UNSUPPORTED;
+        if (d != 16 && d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    } else {
+        if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    }
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (LSE && !aligned16(LSE)))
+        return FA_ERR_MISALIGNED;
+    return FA_OK;
+}
+
+constexpr int kMaxSplits = 64;
+
+// Bytes of split workspace: partial O (fp32) then partial LSE, 256-B aligned.
+long splitkv_bytes(long bh, long N, long d, long S, long* lse_offset) {
+    const long obytes = S * bh * N * d * 4;
+    const long off = (obytes + 255) / 256 * 256;
+    if (lse_offset) *lse_offset = off;
+    return off + S * bh * N * 4;
+}
+
+// Splits that fill the GPU when the (head, query block) units alone do not,
+// keeping at least two key tiles per split.
+int auto_splits(int B, int H, int N, int M) {
+    const long units = (long)((N + 255) / 256) * B * H;
+    const long sms = num_sms();
+    if (sms <= 0 || units >= sms) return 1;
+    long S = (sms + units - 1) / units;
+    const long per = ((long)M + 127) / 128 / 2;
+    if (S > per) S = per;
+    if (S > kMaxSplits) S = kMaxSplits;
+    return S < 1 ? 1 : (int)S;
+}
 }  // namespace
 
 extern "C" {
@@ -119,30 +167,15 @@ const char* fa_status_string(int status) {
 
 int fa_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int M, int d,
                 float scale, int causal, int in_dtype, int out_dtype, void* stream) {
-    if (!Q || !K || !V || !O) return FA_ERR_INVALID_ARG;
-    if (B <= 0 || H <= 0 || N <= 0 || M <= 0 || d <= 0) return FA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-    const long kLim = 1L << 62;
+    const int chk = check_attn_args(Q, K, V, O, LSE, B, H, N, M, d, scale, causal, in_dtype, out_dtype);
+    if (chk != FA_OK) return chk;
     const long bh = (long)B * H;
-    if (!mul_fits(bh, (long)(N > M ? N : M), kLim) || !mul_fits(bh * (N > M ? N : M), d, kLim / 4))
-        return FA_ERR_INVALID_ARG;
-    if (in_dtype != FA_F32 && in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
-    if (out_dtype != FA_F32 && out_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
-    if (bh > 65535) return FA_ERR_UNSUPPORTED;
-    if (in_dtype == FA_F32) {
-        if (out_dtype != FA_F32) return FA_ERR_UNSUPPORTED;
-        if (d != 16 && d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    } else {
-        if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    }
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (LSE && !aligned16(LSE)))
-        return FA_ERR_MISALIGNED;
 
     int err = FA_OK;
     int* status = status_word(&err);
     if (status == nullptr) return err;
-    fa::AttnParams p{Q, K, V, O, LSE, B, H, N, M, d, scale, causal, out_dtype == FA_BF16 ? 1 : 0, status};
+    fa::AttnParams p{Q,     K,      V, O, LSE, B, H, N, M, d, scale, causal, out_dtype == FA_BF16 ? 1 : 0,
+                     status, 1,      nullptr, nullptr};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (in_dtype == FA_F32) {
@@ -154,6 +187,49 @@ int fa_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE
             return FA_ERR_CUDA;
         e = fa::launch_attn_bf16_tc(p, &tq, &tk, &tv, num_sms(), st);
     }
+    return cuda_status(e);
+}
+
+int fa_attn_splitkv_num_splits(int B, int H, int N, int M, int d, int causal) {
+    (void)d;
+    (void)causal;
+    if (B <= 0 || H <= 0 || N <= 0 || M <= 0) return 1;
+    return auto_splits(B, H, N, M);
+}
+
+long fa_attn_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0 || num_splits < 1 || num_splits > kMaxSplits) return -1;
+    if (num_splits == 1) return 0;
+    return splitkv_bytes((long)B * H, N, d, num_splits, nullptr);
+}
+
+int fa_attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int M,
+                        int d, float scale, int causal, int num_splits, void* workspace, long workspace_bytes,
+                        int in_dtype, int out_dtype, void* stream) {
+    const int chk = check_attn_args(Q, K, V, O, LSE, B, H, N, M, d, scale, causal, in_dtype, out_dtype);
+    if (chk != FA_OK) return chk;
+    if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+    const int S = num_splits == 0 ? auto_splits(B, H, N, M) : num_splits;
+    if (S == 1) return fa_attn_fwd(Q, K, V, O, LSE, B, H, N, M, d, scale, causal, in_dtype, out_dtype, stream);
+    if (in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    const long bh = (long)B * H;
+    long loff = 0;
+    const long need = splitkv_bytes(bh, N, d, S, &loff);
+    if (workspace == nullptr || workspace_bytes < need) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_MISALIGNED;
+    int err = FA_OK;
+    int* status = status_word(&err);
+    if (status == nullptr) return err;
+    float* opart = static_cast<float*>(workspace);
+    float* lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + loff);
+    fa::AttnParams p{Q,      K, V, O, LSE, B, H, N, M, d, scale, causal, out_dtype == FA_BF16 ? 1 : 0,
+                     status, S, opart, lpart};
+    CUtensorMap tq, tk, tv;
+    if (!encode_bf16_3d(&tq, Q, bh, N, d) || !encode_bf16_3d(&tk, K, bh, M, d) || !encode_bf16_3d(&tv, V, bh, M, d))
+        return FA_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = fa::launch_attn_bf16_tc(p, &tq, &tk, &tv, num_sms(), st);
+    if (e == cudaSuccess) e = fa::launch_attn_combine(p, st);
     return cuda_status(e);
 }
 

@@ -25,6 +25,9 @@ struct AttnParams {
     int causal;
     int out_bf16;      // 1: O is bf16, 0: O is fp32
     int* status;       // device status word
+    int num_splits;    // > 1: key tiles split over this many CTAs (bf16 path only)
+    float* Opart;      // split partial outputs, fp32 [num_splits][B*H][N][d]
+    float* Lpart;      // split partial LSE, fp32 [num_splits][B*H][N]
 };
 
 // Row-wise kernels (softmax_rows.cu).
@@ -41,6 +44,10 @@ cudaError_t launch_attn_f32(const AttnParams& p, cudaStream_t stream);
 // a 64 x 128 box and 128-byte swizzle.
 cudaError_t launch_attn_bf16_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                 const CUtensorMap* tmV, int num_sms, cudaStream_t stream);
+
+// Combine split partials into O and LSE (attn_splitkv.cu):
+//   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s.
+cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream);
 
 // One CTA waiting on an mbarrier that never completes (attn_tc.cu).
 cudaError_t launch_selftest_wait(int* status, uint64_t limit_ns, cudaStream_t stream);

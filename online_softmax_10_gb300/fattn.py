@@ -25,6 +25,10 @@ _c_int, _c_long, _c_float, _vp = ctypes.c_int, ctypes.c_long, ctypes.c_float, ct
 SIGNATURES = {
     "fa_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
                              _c_int, _c_int, _vp]),
+    "fa_attn_fwd_splitkv": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                     _c_int, _c_int, _vp, _c_long, _c_int, _c_int, _vp]),
+    "fa_attn_splitkv_num_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "fa_attn_splitkv_workspace_bytes": (_c_long, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "fa_softmax_rows": (_c_int, [_vp, _vp, _vp, _c_long, _c_long, _c_int, _c_int, _vp]),
     "fa_logsumexp_rows": (_c_int, [_vp, _vp, _c_long, _c_long, _c_int, _vp]),
     "fa_device_status": (_c_int, [_vp, _c_int]),
@@ -117,6 +121,47 @@ def attn_fwd(q, k, v, scale: float | None = None, causal: bool = False, out_dtyp
                            int(bool(causal)), _dtype_code(q.dtype), _dtype_code(out.dtype), _stream(stream))
     if rc != FA_OK:
         raise FattnError(rc, "fa_attn_fwd")
+    return out, lse
+
+
+def splitkv_num_splits(B: int, H: int, N: int, M: int, d: int, causal: bool) -> int:
+    return lib().fa_attn_splitkv_num_splits(B, H, N, M, d, int(bool(causal)))
+
+
+def splitkv_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int) -> int:
+    return lib().fa_attn_splitkv_workspace_bytes(B, H, N, d, num_splits)
+
+
+def attn_fwd_splitkv(q, k, v, scale: float | None = None, causal: bool = False, num_splits: int = 0,
+                     workspace=None, out_dtype=None, out=None, lse=None, want_lse: bool = True, stream=None):
+    """fa_attn_fwd_splitkv: the key range of each query block split over
+    ``num_splits`` CTAs (0 = automatic), partials merged by a second kernel.
+    ``workspace`` is a caller-owned CUDA byte tensor; allocated here (by torch)
+    when not given."""
+    _check_cuda(q, k, v)
+    B, H, N, d = q.shape
+    M = k.shape[2]
+    if k.shape != (B, H, M, d) or v.shape != (B, H, M, d) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v shapes/dtypes do not match")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    S = num_splits if num_splits > 0 else splitkv_num_splits(B, H, N, M, d, causal)
+    need = splitkv_workspace_bytes(B, H, N, d, S)
+    if need < 0:
+        raise ValueError("invalid split count")
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=out_dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().fa_attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, M, d, float(scale),
+                                   int(bool(causal)), S, _ptr(workspace), wbytes, _dtype_code(q.dtype),
+                                   _dtype_code(out.dtype), _stream(stream))
+    if rc != FA_OK:
+        raise FattnError(rc, "fa_attn_fwd_splitkv")
     return out, lse
 
 

@@ -102,3 +102,26 @@ def test_binding_refuses_cpu_tensors():
         fattn.softmax_rows(x)
     with pytest.raises(ValueError):
         fattn.attn_fwd(torch.zeros(1, 1, 2, 64), torch.zeros(1, 1, 2, 64), torch.zeros(1, 1, 2, 64))
+
+
+def test_splitkv_workspace_bytes_host_arithmetic(L):
+    # partial O fp32 [S][BH][N][d], 256-byte aligned, then partial LSE fp32 [S][BH][N]
+    S, B, H, N, d = 5, 2, 3, 77, 128
+    o = S * B * H * N * d * 4
+    assert L.fa_attn_splitkv_workspace_bytes(B, H, N, d, S) == (o + 255) // 256 * 256 + S * B * H * N * 4
+    assert L.fa_attn_splitkv_workspace_bytes(B, H, N, d, 1) == 0
+    assert L.fa_attn_splitkv_workspace_bytes(B, H, N, d, 0) == -1
+    assert L.fa_attn_splitkv_workspace_bytes(B, H, N, d, 65) == -1
+    assert L.fa_attn_splitkv_workspace_bytes(0, H, N, d, 2) == -1
+
+
+def test_splitkv_argument_errors(L):
+    f = L.fa_attn_fwd_splitkv
+    base = [P, P, P, P, P, 1, 2, 64, 4096, 128, 0.1, 0]
+    assert f(*base, 65, P, 1 << 30, 1, 1, None) == INVALID          # too many splits
+    assert f(*base, -1, P, 1 << 30, 1, 1, None) == INVALID
+    assert f(*base, 4, None, 1 << 30, 1, 1, None) == INVALID        # no workspace
+    assert f(*base, 4, P, 16, 1, 1, None) == INVALID                # workspace too small
+    assert f(*base, 4, P + 16, 1 << 30, 1, 1, None) == MISALIGNED   # not 256-byte aligned
+    assert f(*[P, P, P, P, P, 1, 2, 64, 4096, 64, 0.1, 0], 4, P, 1 << 30, 0, 0, None) == UNSUPPORTED  # fp32 split
+    assert f(None, P, P, P, P, 1, 2, 64, 4096, 128, 0.1, 0, 4, P, 1 << 30, 1, 1, None) == INVALID
