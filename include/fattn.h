@@ -117,6 +117,38 @@ int fa_attn_splitkv_num_splits(int B, int H, int N, int M, int d, int causal);
  * 0 for one split, -1 for invalid arguments.  (No counterpart on the pages.) */
 long fa_attn_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
 
+/* Size of the fixed scratch fa_attn_fwd_splitkv_noalloc uses: 32 MiB. */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * fa_attn_fwd_splitkv_noalloc -- fa_attn_fwd_splitkv for callers that cannot
+ * allocate device memory: code whose device memory is owned by another
+ * allocator (a framework's caching pool, a host program that hands a plugin
+ * only its inputs and outputs), or code that must not call cudaMalloc or
+ * cudaFree, for instance because cudaFree can synchronise the whole device.
+ * Instead of a caller workspace it uses one scratch array of
+ * FA_NOALLOC_SCRATCH_BYTES built into the library, which every GPU that loads
+ * the library holds until the process exits.  It allocates nothing itself.
+ * (The pages have no counterpart: this is a deployment entry point.)
+ *
+ *   Arguments: as fa_attn_fwd_splitkv, without workspace / workspace_bytes.
+ *   Size limit: the split partials, fa_attn_splitkv_workspace_bytes(B, H, N,
+ *       d, S), must fit in FA_NOALLOC_SCRATCH_BYTES; larger problems are
+ *       rejected with FA_ERR_INVALID_ARG before anything is enqueued.
+ *   Set-up: the first call made with a given device current looks up the
+ *       scratch array's device address (cudaGetSymbolAddress) and caches it;
+ *       make that first call before any stream capture.
+ *   Sharing: all calls on a device use the same scratch, which keeps the last
+ *       call's contents (nothing in it needs to start at zero).  Calls that
+ *       overlap on the GPU (other streams, other host threads) race on it;
+ *       the caller must serialise them.
+ * Errors: as fa_attn_fwd_splitkv, FA_ERR_INVALID_ARG for the size limit, and
+ * FA_ERR_CUDA if the scratch address cannot be looked up.
+ */
+int fa_attn_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                int B, int H, int N, int M, int d, float scale, int causal,
+                                int num_splits, int in_dtype, int out_dtype, void* stream);
+
 /*
  * fa_softmax_rows -- P[r, :] = softmax(X[r, :]) and LSE[r] = log sum_c exp X[r, c]
  * for every row, reading X from memory once when a row fits on chip

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["fattn_api.cu", "softmax_rows.cu", "attn_f32.cu", "attn_tc.cu", "attn_splitkv.cu"]
+SOURCES = ["fattn_api.cu", "softmax_rows.cu", "attn_f32.cu", "attn_tc.cu", "attn_splitkv.cu", "attn_noalloc.cu"]
 
 
 def nvcc() -> str:

@@ -27,6 +27,8 @@ SIGNATURES = {
                              _c_int, _c_int, _vp]),
     "fa_attn_fwd_splitkv": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                      _c_int, _c_int, _vp, _c_long, _c_int, _c_int, _vp]),
+    "fa_attn_fwd_splitkv_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                             _c_float, _c_int, _c_int, _c_int, _c_int, _vp]),
     "fa_attn_splitkv_num_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "fa_attn_splitkv_workspace_bytes": (_c_long, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "fa_softmax_rows": (_c_int, [_vp, _vp, _vp, _c_long, _c_long, _c_int, _c_int, _vp]),
@@ -162,6 +164,28 @@ def attn_fwd_splitkv(q, k, v, scale: float | None = None, causal: bool = False, 
                                    _dtype_code(out.dtype), _stream(stream))
     if rc != FA_OK:
         raise FattnError(rc, "fa_attn_fwd_splitkv")
+    return out, lse
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # FA_NOALLOC_SCRATCH_BYTES
+
+
+def attn_fwd_splitkv_noalloc(q, k, v, scale: float | None = None, causal: bool = False, num_splits: int = 0,
+                             out=None, lse=None, stream=None):
+    """fa_attn_fwd_splitkv_noalloc: split-KV attention whose partials go to the
+    library's fixed 32 MiB scratch instead of a caller workspace.  ``out`` and
+    ``lse`` must be given (this call allocates nothing; torch is not asked
+    for memory either)."""
+    _check_cuda(q, k, v, out, lse)
+    B, H, N, d = q.shape
+    M = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = lib().fa_attn_fwd_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, M, d,
+                                           float(scale), int(bool(causal)), int(num_splits), _dtype_code(q.dtype),
+                                           _dtype_code(out.dtype), _stream(stream))
+    if rc != FA_OK:
+        raise FattnError(rc, "fa_attn_fwd_splitkv_noalloc")
     return out, lse
 
 
