@@ -381,7 +381,8 @@ def run_ours(args, world_size, rank, local_rank):
                                      "bytes_per_launch": r_bytes, "peak_source": f"hbm_gbs, {peak_src}"},
                         "launches": rsteps, "l2": "input 268 MB > 129 MB L2, no flush"},
         "logsumexp_rows": {"workload": rw.name, "value": l_bytes / l_per / 1e9, "unit": "GB/s",
-                           "us_per_launch": l_per * 1e6, "frac": l_bytes / l_per / 1e9 / peaks["hbm_gbs"]},
+                           "us_per_launch": l_per * 1e6, "frac": l_bytes / l_per / 1e9 / peaks["hbm_gbs"],
+                           "traffic": recorded_traffic("logsumexp_rows_tma"), "bytes_per_launch": l_bytes},
         "attn_splitkv": {"workload": "attn_bf16_B1_H8_N256_M65536_d128 (decode-like)", "splits": nsplit,
                          "value": s_flops / s_per / 1e12, "unit": "TFLOP/s", "us_per_launch": s_per * 1e6,
                          "unsplit_value": s_flops / u_per / 1e12},
