@@ -104,6 +104,32 @@ def logsumexp_rows(X, nthreads: int | None = None) -> np.ndarray:
     return softmax_rows(X, want_p=False, nthreads=nthreads)[1]
 
 
+def log_softmax_rows(X, nthreads: int | None = None):
+    """log p = z - LSE(z) per row ("从原始Softmax到在线Softmax", section
+    "softmax形式推导", the log-softmax identity).  Returns (logP, LSE)."""
+    X = as_f64(X)
+    lse = logsumexp_rows(X, nthreads)
+    return X - lse[:, None], lse
+
+
+def cross_entropy_rows(X, labels, nthreads: int | None = None):
+    """Per-row cross-entropy -log p_label = LSE(z) - z_label, the log-softmax
+    followed by the label's negative log-probability of the page's
+    cross_entropy_loss sketch ("从原始Softmax到在线Softmax", section
+    "softmax实际代码实现"), without its batch mean.  Labels outside
+    [0, cols) give 0 (an ignored row).  Returns (loss, LSE)."""
+    X = as_f64(X)
+    lab = np.asarray(labels.cpu() if hasattr(labels, "cpu") else labels, dtype=np.int64).reshape(-1)
+    if lab.shape[0] != X.shape[0]:
+        raise ValueError("one label per row")
+    lse = logsumexp_rows(X, nthreads)
+    loss = np.zeros(X.shape[0], dtype=np.float64)
+    ok = (lab >= 0) & (lab < X.shape[1])
+    rows = np.nonzero(ok)[0]
+    loss[rows] = lse[rows] - X[rows, lab[rows]]
+    return loss, lse
+
+
 def attn_fwd(Q, K, V, scale: float, causal: bool = False, rows=None, nthreads: int | None = None):
     """Attention forward in fp64.
 

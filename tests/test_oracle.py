@@ -251,3 +251,32 @@ def test_oracle_rejects_bad_arguments():
     with pytest.raises(RuntimeError):
         oracle.attn_fwd(np.zeros((1, 1, 2, 4)), np.zeros((1, 1, 3, 4)), np.zeros((1, 1, 3, 4)), 1.0,
                         rows=[0, 2])
+
+
+# ---------------------------------------------------------------- log-softmax and cross-entropy
+def test_cross_entropy_printed_value_and_ignored_rows():
+    ex = GOLD["ex2_cross_entropy"]
+    X = np.array([ex["logits"], ex["logits"], ex["logits"]])
+    loss, _ = oracle.cross_entropy_rows(X, [ex["label"], -100, 3])
+    assert abs(loss[0] - ex["loss"]) < TOL
+    assert loss[1] == 0.0 and loss[2] == 0.0
+
+
+def test_cross_entropy_matches_torch_fp64():
+    g = torch.Generator().manual_seed(5)
+    X = torch.randn(37, 1000, generator=g, dtype=torch.float64) * 3
+    lab = torch.randint(0, 1000, (37,), generator=g)
+    loss, lse = oracle.cross_entropy_rows(X, lab)
+    ref = torch.nn.functional.cross_entropy(X, lab, reduction="none").numpy()
+    assert np.max(np.abs(loss - ref)) < 1e-12
+
+
+def test_log_softmax_matches_torch_and_page():
+    g = torch.Generator().manual_seed(6)
+    X = torch.randn(9, 777, generator=g, dtype=torch.float64) * 4
+    lp, lse = oracle.log_softmax_rows(X)
+    assert np.max(np.abs(lp - torch.log_softmax(X, -1).numpy())) < 1e-12
+    assert np.max(np.abs(np.exp(lp).sum(1) - 1)) < 1e-12
+    ex = GOLD["ex1_softmax"]
+    lp1, _ = oracle.log_softmax_rows(np.array([ex["logits"]]))
+    assert np.max(np.abs(np.exp(lp1[0]) - ex["p"])) < TOL
