@@ -185,6 +185,39 @@ int fa_logsumexp_rows(const void* X, float* LSE, long rows, long cols,
                       int in_dtype, void* stream);
 
 /*
+ * fa_log_softmax_rows -- Y[r, :] = log softmax(X[r, :]) = X[r, :] - LSE[r],
+ * the log-softmax identity log p_j = z_j - LSE(z) of "从原始Softmax到在线Softmax",
+ * section "softmax形式推导", with LSE from the same online reduction as
+ * fa_softmax_rows (one read of X when a row fits on chip).
+ *
+ *   X    [rows, cols]  row-major, FA_BF16 or FA_F32
+ *   Y    [rows, cols]  row-major, FA_BF16 or FA_F32, written; must not overlap X
+ *   LSE  [rows]        fp32, written; may be NULL
+ * Errors: as fa_softmax_rows.
+ */
+int fa_log_softmax_rows(const void* X, void* Y, float* LSE, long rows, long cols,
+                        int in_dtype, int out_dtype, void* stream);
+
+/*
+ * fa_cross_entropy_rows -- per-row cross-entropy of logits X against integer
+ * labels: loss[r] = LSE(X[r, :]) - X[r, labels[r]] = -log softmax(X[r, :])[label],
+ * the log-softmax-then-negative-log-likelihood of the cross_entropy_loss sketch
+ * on "从原始Softmax到在线Softmax" (section "softmax实际代码实现"; worked example 2
+ * gives 0.4170), fused into the log-sum-exp pass: one read of X.  The batch
+ * mean of that sketch is left to the caller.
+ *
+ *   X       [rows, cols]  row-major logits, FA_BF16 or FA_F32
+ *   labels  [rows]        int64 class indices; a label outside [0, cols)
+ *                         (e.g. -100) marks an ignored row whose loss is 0
+ *   loss    [rows]        fp32, written; must not be NULL
+ *   LSE     [rows]        fp32, written; may be NULL
+ * Errors: FA_ERR_INVALID_ARG for NULL X/labels/loss or bad sizes;
+ * FA_ERR_UNSUPPORTED for other dtypes; FA_ERR_MISALIGNED; FA_ERR_CUDA.
+ */
+int fa_cross_entropy_rows(const void* X, const long long* labels, float* loss, float* LSE,
+                          long rows, long cols, int in_dtype, void* stream);
+
+/*
  * fa_device_status -- synchronise `stream`, then return FA_OK or the first
  * error a kernel recorded on the current device since the last reset
  * (FA_ERR_DEVICE_TIMEOUT), or FA_ERR_CUDA if the synchronisation itself

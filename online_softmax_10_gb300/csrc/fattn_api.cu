@@ -233,8 +233,10 @@ int fa_attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, fl
     return cuda_status(e);
 }
 
-int fa_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, int in_dtype, int out_dtype,
-                    void* stream) {
+namespace {
+
+int softmax_rows_impl(const void* X, void* P, float* LSE, long rows, long cols, int in_dtype, int out_dtype,
+                      int log_out, void* stream) {
     if (!X || !P) return FA_ERR_INVALID_ARG;
     if (rows <= 0 || cols <= 0 || !mul_fits(rows, cols, 1L << 60)) return FA_ERR_INVALID_ARG;
     if ((in_dtype != FA_F32 && in_dtype != FA_BF16) || (out_dtype != FA_F32 && out_dtype != FA_BF16))
@@ -244,21 +246,46 @@ int fa_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, in
     int* status = status_word(&err);
     if (status == nullptr) return err;
     const cudaError_t e = fa::launch_softmax_rows(X, P, LSE, rows, cols, in_dtype == FA_BF16, out_dtype == FA_BF16,
-                                                  status, static_cast<cudaStream_t>(stream));
+                                                  log_out, status, static_cast<cudaStream_t>(stream));
     return cuda_status(e);
 }
 
-int fa_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_dtype, void* stream) {
-    if (!X || !LSE) return FA_ERR_INVALID_ARG;
+int lse_rows_impl(const void* X, const long long* labels, float* loss, float* LSE, long rows, long cols,
+                  int in_dtype, void* stream) {
+    if (!X || (!LSE && !loss) || (loss && !labels)) return FA_ERR_INVALID_ARG;
     if (rows <= 0 || cols <= 0 || !mul_fits(rows, cols, 1L << 60)) return FA_ERR_INVALID_ARG;
     if (in_dtype != FA_F32 && in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
-    if (!aligned16(X) || !aligned16(LSE)) return FA_ERR_MISALIGNED;
+    if (!aligned16(X) || (LSE && !aligned16(LSE)) || (loss && !aligned16(loss)) || (labels && !aligned16(labels)))
+        return FA_ERR_MISALIGNED;
     int err = FA_OK;
     int* status = status_word(&err);
     if (status == nullptr) return err;
-    const cudaError_t e = fa::launch_logsumexp_rows(X, LSE, rows, cols, in_dtype == FA_BF16, status,
+    const cudaError_t e = fa::launch_logsumexp_rows(X, LSE, rows, cols, in_dtype == FA_BF16, labels, loss, status,
                                                     static_cast<cudaStream_t>(stream));
     return cuda_status(e);
+}
+
+}  // namespace
+
+int fa_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, int in_dtype, int out_dtype,
+                    void* stream) {
+    return softmax_rows_impl(X, P, LSE, rows, cols, in_dtype, out_dtype, 0, stream);
+}
+
+int fa_log_softmax_rows(const void* X, void* Y, float* LSE, long rows, long cols, int in_dtype, int out_dtype,
+                        void* stream) {
+    return softmax_rows_impl(X, Y, LSE, rows, cols, in_dtype, out_dtype, 1, stream);
+}
+
+int fa_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_dtype, void* stream) {
+    if (!LSE) return FA_ERR_INVALID_ARG;
+    return lse_rows_impl(X, nullptr, nullptr, LSE, rows, cols, in_dtype, stream);
+}
+
+int fa_cross_entropy_rows(const void* X, const long long* labels, float* loss, float* LSE, long rows, long cols,
+                          int in_dtype, void* stream) {
+    if (!loss || !labels) return FA_ERR_INVALID_ARG;
+    return lse_rows_impl(X, labels, loss, LSE, rows, cols, in_dtype, stream);
 }
 
 int fa_device_status(void* stream, int reset) {

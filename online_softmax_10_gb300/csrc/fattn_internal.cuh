@@ -31,10 +31,13 @@ struct AttnParams {
 };
 
 // Row-wise kernels (softmax_rows.cu).
+// log_out: write log p = x - LSE instead of p.
 cudaError_t launch_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, int in_bf16,
-                                int out_bf16, int* status, cudaStream_t stream);
-cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_bf16, int* status,
-                                  cudaStream_t stream);
+                                int out_bf16, int log_out, int* status, cudaStream_t stream);
+// LSE (may be null when loss is given); labels/loss: the fused cross-entropy
+// loss[r] = LSE[r] - X[r, labels[r]] (0 outside [0, cols)), or both null.
+cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_bf16,
+                                  const long long* labels, float* loss, int* status, cudaStream_t stream);
 
 // fp32 CUDA-core attention (attn_f32.cu).  d in {16, 32, 64, 128}.
 cudaError_t launch_attn_f32(const AttnParams& p, cudaStream_t stream);

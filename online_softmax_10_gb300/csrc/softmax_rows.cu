@@ -116,6 +116,19 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2)
     m = M;
 }
 
+// Row results of the log-sum-exp kernels: LSE (if wanted) and, for the fused
+// cross-entropy, loss = LSE - x[label] (0 for a label outside [0, cols)).
+template <typename TIn>
+__device__ __forceinline__ void write_row_lse(const TIn* __restrict__ X, long row, long cols, float lse,
+                                              float* __restrict__ LSE, const long long* __restrict__ labels,
+                                              float* __restrict__ loss) {
+    if (LSE != nullptr) LSE[row] = lse;
+    if (loss != nullptr) {
+        const long long lab = labels[row];
+        loss[row] = (lab >= 0 && lab < cols) ? lse - Elem<TIn>::load1(X + row * cols + lab) : 0.f;
+    }
+}
+
 // Merge (m, s) across the CTA; every thread receives the row's (M, S).
 template <int THREADS>
 __device__ __forceinline__ void block_merge(float& m, float& s, float* sm_m, float* sm_s) {
@@ -143,7 +156,7 @@ __device__ __forceinline__ void block_merge(float& m, float& s, float* sm_m, flo
 }
 
 // One CTA per row (grid-strided); the row lives in registers.
-template <typename TIn, typename TOut, int THREADS, int NV>
+template <typename TIn, typename TOut, int THREADS, int NV, bool LOGP>
 __global__ void __launch_bounds__(THREADS) softmax_rows_resident(const TIn* __restrict__ X, TOut* __restrict__ P,
                                                                  float* __restrict__ LSE, long rows, long cols,
                                                                  int vec_ok) {
@@ -179,8 +192,9 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_resident(const TIn* __re
             s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
         block_merge<THREADS>(m, s, sm_m, sm_s);
-        // p = exp(x - M) / S = 2^((x - M) log2e - log2 S)
+        // p = exp(x - M) / S = 2^((x - M) log2e - log2 S);  log p = x - (M + ln S)
         const float l2s = __log2f(s);
+        const float lse_row = m + logf(s);
         TOut* p = P + row * cols;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -188,7 +202,7 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_resident(const TIn* __re
             if (e0 < cols) {
                 float o[V];
 #pragma unroll
-                for (int i = 0; i < V; ++i) o[i] = ex2(fmaf(v[k][i] - m, kLog2e, -l2s));
+                for (int i = 0; i < V; ++i) o[i] = LOGP ? v[k][i] - lse_row : ex2(fmaf(v[k][i] - m, kLog2e, -l2s));
                 const int valid = (int)((cols - e0) < V ? (cols - e0) : V);
                 store_out<TOut, V>(p + e0, o, vec_ok && valid == V, valid);
             }
@@ -236,19 +250,21 @@ __device__ __forceinline__ void row_online_ms(const TIn* __restrict__ x, long co
 
 template <typename TIn, int THREADS, int U>
 __global__ void __launch_bounds__(THREADS) logsumexp_rows_stream(const TIn* __restrict__ X, float* __restrict__ LSE,
-                                                                 long rows, long cols, int vec_ok) {
+                                                                 long rows, long cols, int vec_ok,
+                                                                 const long long* __restrict__ labels,
+                                                                 float* __restrict__ loss) {
     __shared__ float sm_m[32], sm_s[32];
     for (long row = blockIdx.x; row < rows; row += gridDim.x) {
         float m, s;
         row_online_ms<TIn, THREADS, U>(X + row * cols, cols, vec_ok != 0, m, s);
         block_merge<THREADS>(m, s, sm_m, sm_s);
-        if (threadIdx.x == 0) LSE[row] = m + logf(s);
+        if (threadIdx.x == 0) write_row_lse(X, row, cols, m + logf(s), LSE, labels, loss);
     }
 }
 
 // Rows longer than the resident capacity: online reduction pass, then a second
 // read of the row to write P.
-template <typename TIn, typename TOut, int THREADS, int U>
+template <typename TIn, typename TOut, int THREADS, int U, bool LOGP>
 __global__ void __launch_bounds__(THREADS) softmax_rows_stream(const TIn* __restrict__ X, TOut* __restrict__ P,
                                                                float* __restrict__ LSE, long rows, long cols,
                                                                int vec_ok) {
@@ -260,6 +276,7 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_stream(const TIn* __rest
         row_online_ms<TIn, THREADS, U>(x, cols, vec_ok != 0, m, s);
         block_merge<THREADS>(m, s, sm_m, sm_s);
         const float l2s = __log2f(s);
+        const float lse_row = m + logf(s);
         TOut* p = P + row * cols;
         const long nvec = (cols + V - 1) / V;
         for (long vi = threadIdx.x; vi < nvec; vi += THREADS) {
@@ -272,7 +289,7 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_stream(const TIn* __rest
                 for (int i = 0; i < V; ++i) f[i] = i < valid ? Elem<TIn>::load1(x + e0 + i) : 0.f;
             }
 #pragma unroll
-            for (int i = 0; i < V; ++i) f[i] = ex2(fmaf(f[i] - m, kLog2e, -l2s));
+            for (int i = 0; i < V; ++i) f[i] = LOGP ? f[i] - lse_row : ex2(fmaf(f[i] - m, kLog2e, -l2s));
             store_out<TOut, V>(p + e0, f, vec_ok && valid == V, valid);
         }
         if (LSE != nullptr && threadIdx.x == 0) LSE[row] = m + logf(s);
@@ -290,7 +307,7 @@ constexpr uint32_t kTmaSmemExtra = 128 /* alignment */ + kTmaBarBytes + 2 * 16 *
 
 // One CTA per SM; rows r = blockIdx.x + i * gridDim.x go through a ring of
 // `nst` shared-memory stages of `stage_bytes` each.
-template <typename TIn, typename TOut, bool WRITE_P, int NV>
+template <typename TIn, typename TOut, bool WRITE_P, int NV, bool LOGP>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restrict__ LSE, long rows, long cols,
                  uint32_t stage_bytes, int nst, int* status) {
@@ -404,7 +421,7 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
                     const float ex = ex2((v[k][e] - m) * kc);
-                    if (WRITE_P) v[k][e] = ex;
+                    if (WRITE_P && !LOGP) v[k][e] = ex;  // log p keeps x itself
                     acc[e & 3] += ex;
                 }
             sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
@@ -442,8 +459,9 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
             }
         }
         if (WRITE_P) {
-            // p = exp(x - m) * exp(m - M) / S
+            // p = exp(x - m) * exp(m - M) / S;  log p = x - (M + ln S)
             const float f = m == -CUDART_INF_F ? 0.f : ex2((m - M) * kc) / S;
+            const float lse_row = M + logf(S);
             TOut* prow = P + r * cols;
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
@@ -451,7 +469,7 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
                 if (vi < nvec) {
                     float o[V];
 #pragma unroll
-                    for (int e = 0; e < V; ++e) o[e] = v[k][e] * f;
+                    for (int e = 0; e < V; ++e) o[e] = LOGP ? v[k][e] - lse_row : v[k][e] * f;
                     store_out<TOut, V>(prow + vi * V, o, true, V);
                 }
             }
@@ -475,7 +493,7 @@ constexpr int kLseGroupThreads = kTmaConsumers / kLseGroups;  // 256
 template <typename TIn, int NV>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows, long cols, uint32_t stage_bytes,
-                   int nst, int* status) {
+                   int nst, int* status, const long long* __restrict__ labels, float* __restrict__ loss) {
     constexpr int V = Elem<TIn>::kVec;
     constexpr int WG = kLseGroupThreads / 32;  // warps per group
     constexpr int CH = 4;                      // vectors per online step
@@ -634,7 +652,7 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
                 const float s2 = __shfl_xor_sync(0xFFFFFFFFu, S, off);
                 merge_ms(M, S, m2, s2);
             }
-            if (lane == 0) LSE[r] = M + logf(S);
+            if (lane == 0) write_row_lse(X, r, cols, M + logf(S), LSE, labels, loss);
         }
     }
 }
@@ -647,7 +665,7 @@ int device_sms() {
 }
 
 // Launch the pipelined kernel if the row shape suits it; returns false if not.
-template <typename TIn, typename TOut, bool WRITE_P>
+template <typename TIn, typename TOut, bool WRITE_P, bool LOGP>
 bool try_launch_tma(const TIn* X, TOut* P, float* LSE, long rows, long cols, int* status, cudaStream_t st,
                     cudaError_t* err) {
     constexpr int V = Elem<TIn>::kVec;
@@ -667,9 +685,9 @@ bool try_launch_tma(const TIn* X, TOut* P, float* LSE, long rows, long cols, int
         }
         *err = e;
     };
-    if (nvec <= 2L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 2>);
-    else if (nvec <= 4L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4>);
-    else launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8>);
+    if (nvec <= 2L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 2, LOGP>);
+    else if (nvec <= 4L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4, LOGP>);
+    else launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP>);
     return true;
 }
 
@@ -677,7 +695,7 @@ bool try_launch_tma(const TIn* X, TOut* P, float* LSE, long rows, long cols, int
 // Launch the pipelined LSE-only kernel if the row shape suits it.
 template <typename TIn>
 bool try_launch_lse_tma(const TIn* X, float* LSE, long rows, long cols, int* status, cudaStream_t st,
-                        cudaError_t* err) {
+                        cudaError_t* err, const long long* labels, float* loss) {
     constexpr int V = Elem<TIn>::kVec;
     const long row_bytes = cols * (long)sizeof(TIn);
     if (cols % V != 0 || row_bytes < 16384 || row_bytes > 65536 || rows < 64) return false;
@@ -691,7 +709,7 @@ bool try_launch_lse_tma(const TIn* X, float* LSE, long rows, long cols, int* sta
     auto launch = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess) {
-            kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(X, LSE, rows, cols, stage, nst, status);
+            kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(X, LSE, rows, cols, stage, nst, status, labels, loss);
             e = cudaGetLastError();
         }
         *err = e;
@@ -706,16 +724,16 @@ long grid_for_rows(long rows) {
     return rows < kMaxGrid ? rows : kMaxGrid;
 }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool LOGP>
 cudaError_t softmax_dispatch(const TIn* X, TOut* P, float* LSE, long rows, long cols, int* status,
                              cudaStream_t st) {
     constexpr int V = Elem<TIn>::kVec;
     cudaError_t terr;
-    if (try_launch_tma<TIn, TOut, true>(X, P, LSE, rows, cols, status, st, &terr)) return terr;
+    if (try_launch_tma<TIn, TOut, true, LOGP>(X, P, LSE, rows, cols, status, st, &terr)) return terr;
     const int vec_ok = (cols % V) == 0;
     const long nvec = (cols + V - 1) / V;
     const dim3 grid((unsigned)grid_for_rows(rows));
-#define FA_RESIDENT(T, NVV) softmax_rows_resident<TIn, TOut, T, NVV><<<grid, T, 0, st>>>(X, P, LSE, rows, cols, vec_ok)
+#define FA_RESIDENT(T, NVV) softmax_rows_resident<TIn, TOut, T, NVV, LOGP><<<grid, T, 0, st>>>(X, P, LSE, rows, cols, vec_ok)
     if (nvec <= 32) FA_RESIDENT(32, 1);
     else if (nvec <= 64) FA_RESIDENT(32, 2);
     else if (nvec <= 128) FA_RESIDENT(32, 4);
@@ -725,43 +743,45 @@ cudaError_t softmax_dispatch(const TIn* X, TOut* P, float* LSE, long rows, long 
     else if (nvec <= 2048) FA_RESIDENT(256, 8);
     else if (nvec <= 4096) FA_RESIDENT(512, 8);
     else if (nvec <= 8192) FA_RESIDENT(1024, 8);
-    else softmax_rows_stream<TIn, TOut, 512, 4><<<grid, 512, 0, st>>>(X, P, LSE, rows, cols, vec_ok);
+    else softmax_rows_stream<TIn, TOut, 512, 4, LOGP><<<grid, 512, 0, st>>>(X, P, LSE, rows, cols, vec_ok);
 #undef FA_RESIDENT
     return cudaGetLastError();
 }
 
 template <typename TIn>
-cudaError_t lse_dispatch(const TIn* X, float* LSE, long rows, long cols, int* status, cudaStream_t st) {
+cudaError_t lse_dispatch(const TIn* X, float* LSE, long rows, long cols, int* status, cudaStream_t st,
+                         const long long* labels, float* loss) {
     constexpr int V = Elem<TIn>::kVec;
     cudaError_t terr;
-    if (try_launch_lse_tma<TIn>(X, LSE, rows, cols, status, st, &terr)) return terr;
+    if (try_launch_lse_tma<TIn>(X, LSE, rows, cols, status, st, &terr, labels, loss)) return terr;
     const int vec_ok = (cols % V) == 0;
     const long nvec = (cols + V - 1) / V;
     const dim3 grid((unsigned)grid_for_rows(rows));
-    if (nvec <= 128) logsumexp_rows_stream<TIn, 32, 4><<<grid, 32, 0, st>>>(X, LSE, rows, cols, vec_ok);
-    else if (nvec <= 1024) logsumexp_rows_stream<TIn, 128, 4><<<grid, 128, 0, st>>>(X, LSE, rows, cols, vec_ok);
-    else logsumexp_rows_stream<TIn, 512, 4><<<grid, 512, 0, st>>>(X, LSE, rows, cols, vec_ok);
+    if (nvec <= 128) logsumexp_rows_stream<TIn, 32, 4><<<grid, 32, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
+    else if (nvec <= 1024) logsumexp_rows_stream<TIn, 128, 4><<<grid, 128, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
+    else logsumexp_rows_stream<TIn, 512, 4><<<grid, 512, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_softmax_rows(const void* X, void* P, float* LSE, long rows, long cols, int in_bf16, int out_bf16,
-                                int* status, cudaStream_t st) {
+                                int log_out, int* status, cudaStream_t st) {
     using bf = __nv_bfloat16;
-    if (in_bf16 && out_bf16)
-        return softmax_dispatch((const bf*)X, (bf*)P, LSE, rows, cols, status, st);
-    if (in_bf16)
-        return softmax_dispatch((const bf*)X, (float*)P, LSE, rows, cols, status, st);
-    if (out_bf16)
-        return softmax_dispatch((const float*)X, (bf*)P, LSE, rows, cols, status, st);
-    return softmax_dispatch((const float*)X, (float*)P, LSE, rows, cols, status, st);
+#define FA_SOFTMAX(TI, TO)                                                                            \
+    return log_out ? softmax_dispatch<TI, TO, true>((const TI*)X, (TO*)P, LSE, rows, cols, status, st) \
+                   : softmax_dispatch<TI, TO, false>((const TI*)X, (TO*)P, LSE, rows, cols, status, st)
+    if (in_bf16 && out_bf16) { FA_SOFTMAX(bf, bf); }
+    if (in_bf16) { FA_SOFTMAX(bf, float); }
+    if (out_bf16) { FA_SOFTMAX(float, bf); }
+    FA_SOFTMAX(float, float);
+#undef FA_SOFTMAX
 }
 
-cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_bf16, int* status,
-                                  cudaStream_t st) {
-    if (in_bf16) return lse_dispatch((const __nv_bfloat16*)X, LSE, rows, cols, status, st);
-    return lse_dispatch((const float*)X, LSE, rows, cols, status, st);
+cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long cols, int in_bf16,
+                                  const long long* labels, float* loss, int* status, cudaStream_t st) {
+    if (in_bf16) return lse_dispatch((const __nv_bfloat16*)X, LSE, rows, cols, status, st, labels, loss);
+    return lse_dispatch((const float*)X, LSE, rows, cols, status, st, labels, loss);
 }
 
 }  // namespace fa

@@ -33,6 +33,8 @@ SIGNATURES = {
     "fa_attn_splitkv_workspace_bytes": (_c_long, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "fa_softmax_rows": (_c_int, [_vp, _vp, _vp, _c_long, _c_long, _c_int, _c_int, _vp]),
     "fa_logsumexp_rows": (_c_int, [_vp, _vp, _c_long, _c_long, _c_int, _vp]),
+    "fa_log_softmax_rows": (_c_int, [_vp, _vp, _vp, _c_long, _c_long, _c_int, _c_int, _vp]),
+    "fa_cross_entropy_rows": (_c_int, [_vp, _vp, _vp, _vp, _c_long, _c_long, _c_int, _vp]),
     "fa_device_status": (_c_int, [_vp, _c_int]),
     "fa_selftest_wait_timeout": (_c_int, [_c_int, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),
@@ -203,6 +205,40 @@ def softmax_rows(x, out_dtype=None, out=None, lse=None, want_lse: bool = True, s
     if rc != FA_OK:
         raise FattnError(rc, "fa_softmax_rows")
     return out, lse
+
+
+def log_softmax_rows(x, out_dtype=None, out=None, lse=None, want_lse: bool = True, stream=None):
+    """Row-wise log-softmax of a 2-D CUDA tensor through fa_log_softmax_rows. Returns (logp, lse)."""
+    _check_cuda(x)
+    rows, cols = x.shape
+    out_dtype = out_dtype or x.dtype
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype, device=x.device)
+    if lse is None and want_lse:
+        lse = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    rc = lib().fa_log_softmax_rows(_ptr(x), _ptr(out), _ptr(lse), rows, cols, _dtype_code(x.dtype),
+                                   _dtype_code(out.dtype), _stream(stream))
+    if rc != FA_OK:
+        raise FattnError(rc, "fa_log_softmax_rows")
+    return out, lse
+
+
+def cross_entropy_rows(x, labels, loss=None, lse=None, want_lse: bool = False, stream=None):
+    """Per-row cross-entropy LSE(x_r) - x_r[label_r] through fa_cross_entropy_rows
+    (int64 labels; labels outside [0, cols) give 0).  Returns (loss, lse)."""
+    _check_cuda(x, labels)
+    if labels.dtype != torch.int64:
+        raise TypeError("labels must be int64")
+    rows, cols = x.shape
+    if loss is None:
+        loss = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    if lse is None and want_lse:
+        lse = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    rc = lib().fa_cross_entropy_rows(_ptr(x), _ptr(labels), _ptr(loss), _ptr(lse), rows, cols,
+                                     _dtype_code(x.dtype), _stream(stream))
+    if rc != FA_OK:
+        raise FattnError(rc, "fa_cross_entropy_rows")
+    return loss, lse
 
 
 def logsumexp_rows(x, out=None, stream=None):

@@ -125,3 +125,15 @@ def test_splitkv_argument_errors(L):
     assert f(*base, 4, P + 16, 1 << 30, 1, 1, None) == MISALIGNED   # not 256-byte aligned
     assert f(*[P, P, P, P, P, 1, 2, 64, 4096, 64, 0.1, 0], 4, P, 1 << 30, 0, 0, None) == UNSUPPORTED  # fp32 split
     assert f(None, P, P, P, P, 1, 2, 64, 4096, 128, 0.1, 0, 4, P, 1 << 30, 1, 1, None) == INVALID
+
+
+def test_row_extras_argument_errors(L):
+    assert L.fa_log_softmax_rows(None, P, P, 4, 8, 1, 1, None) == INVALID
+    assert L.fa_log_softmax_rows(P, None, P, 4, 8, 1, 1, None) == INVALID
+    assert L.fa_log_softmax_rows(P, P + 8, P, 4, 8, 1, 1, None) == MISALIGNED
+    assert L.fa_log_softmax_rows(P, P, P, 4, 8, 1, 7, None) == UNSUPPORTED
+    assert L.fa_cross_entropy_rows(P, None, P, P, 4, 8, 1, None) == INVALID   # no labels
+    assert L.fa_cross_entropy_rows(P, P, None, P, 4, 8, 1, None) == INVALID   # no loss
+    assert L.fa_cross_entropy_rows(P, P, P, P, 0, 8, 1, None) == INVALID
+    assert L.fa_cross_entropy_rows(P, P + 8, P, None, 4, 8, 1, None) == MISALIGNED
+    assert L.fa_cross_entropy_rows(P, P, P, None, 4, 8, 3, None) == UNSUPPORTED
