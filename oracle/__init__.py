@@ -130,8 +130,10 @@ def cross_entropy_rows(X, labels, nthreads: int | None = None):
     return loss, lse
 
 
-def attn_fwd(Q, K, V, scale: float, causal: bool = False, rows=None, nthreads: int | None = None):
-    """Attention forward in fp64.
+def attn_fwd(Q, K, V, scale: float, causal=False, rows=None, nthreads: int | None = None):
+    """Attention forward in fp64.  causal: 0/False none, 1/True top-left
+    (key j for query i iff j <= i), 2 bottom-right (iff j <= i + M - N); a
+    query with no kept key gets O = 0, LSE = -inf.
 
     Q [B,H,N,d], K [B,H,M,d], V [B,H,M,d] (numpy or CPU torch; widened exactly).
     ``rows``: optional 1-D array of flat query indices (b*H + h)*N + i.
@@ -155,7 +157,7 @@ def attn_fwd(Q, K, V, scale: float, causal: bool = False, rows=None, nthreads: i
         sel_p = sel.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
     O = np.empty((nsel, d), dtype=np.float64)
     LSE = np.empty(nsel, dtype=np.float64)
-    rc = lib.oracle_attn_rows(_dptr(Q), _dptr(K), _dptr(V), B, H, N, M, d, float(scale), int(bool(causal)),
+    rc = lib.oracle_attn_rows(_dptr(Q), _dptr(K), _dptr(V), B, H, N, M, d, float(scale), int(causal),
                               sel_p, nsel, _dptr(O), _dptr(LSE), nthreads or default_threads())
     if rc != 0:
         raise RuntimeError(f"oracle_attn_rows failed ({rc})")

@@ -23,8 +23,11 @@
  *     "Attention的数学表达", eq (8)-(9) (Q[N,K], K[M,K], V[M,K], A[N,K]):
  *         x_j = scale * sum_k Q[i,k] K[j,k]     for every key j that is kept,
  *         O[i,:] = sum_j p_j V[j,:],            LSE[i] = m + log s.
- *     The causal mask keeps key j for query i iff j <= i (top-left aligned; the
- *     pages leave the mask's form open and this is the plainest reading).
+ *     The causal mask keeps key j for query i iff j <= i (causal = 1, top-left
+ *     aligned; the pages leave the mask's form open and this is the plainest
+ *     reading) or iff j <= i + (M - N) (causal = 2, bottom-right aligned, the
+ *     last query sees every key).  A query with no kept key has O = 0 and
+ *     LSE = -inf (a convention: the definition is empty there).
  *
  * Every sum runs in index order in double precision; no blocking, fusion or
  * reordering.  Rows are independent, so they are spread over POSIX threads;
@@ -160,9 +163,22 @@ static void *attn_worker(void *arg)
         const double *q = job->Q + flat * d;
         const double *Kh = job->K + bh * M * d;
         const double *Vh = job->V + bh * M * d;
-        /* keys kept for this query: all M, or 0..i under the causal mask */
+        /* keys kept for this query: all M; 0..i under the top-left causal mask
+         * (causal = 1); 0..i+(M-N) under the bottom-right one (causal = 2) */
         long kept = M;
-        if (job->causal && i + 1 < M) kept = i + 1;
+        if (job->causal == 1 && i + 1 < M) kept = i + 1;
+        if (job->causal == 2) {
+            long last = i + (M - N);            /* last kept key */
+            kept = last + 1 < M ? last + 1 : M;
+            if (kept < 0) kept = 0;
+        }
+        double *o = job->O + t * d;
+        if (kept == 0) {
+            /* no key is kept: O = 0 and LSE = -inf by convention */
+            for (long c = 0; c < d; ++c) o[c] = 0.0;
+            if (job->LSE) job->LSE[t] = -INFINITY;
+            continue;
+        }
         /* materialise the score row x_j = scale * (q . k_j) */
         for (long j = 0; j < kept; ++j) {
             const double *k = Kh + j * d;
@@ -173,7 +189,6 @@ static void *attn_worker(void *arg)
         /* P = softmax(x) by the three passes, then O = P V */
         double lse;
         softmax_three_pass(x, kept, p, &lse);
-        double *o = job->O + t * d;
         for (long c = 0; c < d; ++c) o[c] = 0.0;
         for (long j = 0; j < kept; ++j) {
             const double *v = Vh + j * d;
@@ -200,6 +215,7 @@ int oracle_attn_rows(const double *Q, const double *K, const double *V,
 {
     if (!Q || !K || !V || !O) return -1;
     if (B <= 0 || H <= 0 || N <= 0 || M <= 0 || d <= 0 || nsel < 0) return -1;
+    if (causal < 0 || causal > 2) return -1;
     if (!sel && nsel != B * H * N) return -1;
     if (sel)
         for (long t = 0; t < nsel; ++t)

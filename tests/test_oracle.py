@@ -280,3 +280,32 @@ def test_log_softmax_matches_torch_and_page():
     ex = GOLD["ex1_softmax"]
     lp1, _ = oracle.log_softmax_rows(np.array([ex["logits"]]))
     assert np.max(np.abs(np.exp(lp1[0]) - ex["p"])) < TOL
+
+
+# ---------------------------------------------------------------- bottom-right causal
+@pytest.mark.parametrize("N,M", [(9, 31), (31, 9), (17, 17), (1, 40), (40, 1)])
+def test_bottom_right_causal_matches_torch_masked_fp64(N, M):
+    rng = np.random.default_rng(N * 100 + M)
+    Q, K, V = rng.normal(size=(2, 2, N, 16)), rng.normal(size=(2, 2, M, 16)), rng.normal(size=(2, 2, M, 16))
+    O, lse = oracle.attn_fwd(Q, K, V, 0.25, 2)
+    keep = torch.ones(N, M, dtype=torch.bool).tril(diagonal=M - N)   # key j kept iff j <= i + (M - N)
+    has = keep.any(1).numpy()
+    S = torch.einsum("bhnd,bhmd->bhnm", torch.tensor(Q), torch.tensor(K)) * 0.25
+    S = S.masked_fill(~keep, -math.inf)
+    if has.any():
+        P = torch.softmax(S[:, :, has], -1)
+        ref = torch.einsum("bhnm,bhmd->bhnd", P, torch.tensor(V)).numpy()
+        assert np.max(np.abs(O[:, :, has] - ref)) < 1e-12
+        assert np.max(np.abs(lse[:, :, has] - torch.logsumexp(S[:, :, has], -1).numpy())) < 1e-12
+    # rows with no kept key: O = 0, LSE = -inf
+    assert np.all(O[:, :, ~has] == 0) and np.all(np.isneginf(lse[:, :, ~has]))
+
+
+def test_bottom_right_equals_top_left_when_square_and_last_row_sees_all():
+    rng = np.random.default_rng(2)
+    Q, K, V = (rng.normal(size=(1, 1, 12, 8)) for _ in range(3))
+    assert np.array_equal(oracle.attn_fwd(Q, K, V, 0.3, 2)[0], oracle.attn_fwd(Q, K, V, 0.3, 1)[0])
+    K2, V2 = rng.normal(size=(1, 1, 30, 8)), rng.normal(size=(1, 1, 30, 8))
+    O_br, _ = oracle.attn_fwd(Q, K2, V2, 0.3, 2)
+    O_all, _ = oracle.attn_fwd(Q, K2, V2, 0.3, 0)
+    assert np.max(np.abs(O_br[0, 0, -1] - O_all[0, 0, -1])) < 1e-15
