@@ -67,7 +67,9 @@ typedef enum fa_status {
  *                      the keys kept for row i (written; may be NULL = skip)
  *   scale  multiplier of Q K^T (finite, non-zero), usually 1/sqrt(d)
  *   causal 0: every key is kept; 1: key j is kept for query i iff j <= i
- *          (top-left aligned, also when N != M)
+ *          (top-left aligned, also when N != M); 2: iff j <= i + (M - N)
+ *          (bottom-right aligned: the last query sees every key).  A query
+ *          that keeps no key (causal = 2 with N > M) gets O = 0, LSE = -inf.
  *   in_dtype / out_dtype:
  *      FA_BF16 in  -> tensor-core path, d in {64, 128}; out FA_BF16 or FA_F32
  *      FA_F32  in  -> fp32 CUDA-core path, d in {16, 32, 64, 128}; out FA_F32
@@ -78,6 +80,23 @@ typedef enum fa_status {
 int fa_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                 int B, int H, int N, int M, int d, float scale, int causal,
                 int in_dtype, int out_dtype, void* stream);
+
+/*
+ * fa_attn_fwd_strided -- fa_attn_fwd on tensors with arbitrary batch, head and
+ * row strides (e.g. the [B, N, H, d] layout), d contiguous in every tensor.
+ *
+ *   q_stride, k_stride, v_stride, o_stride: 3 element strides each, in the
+ *       order (batch, head, row); positive, and each a multiple of 16 bytes.
+ *       [B, H, N, d] is {H*N*d, N*d, d}; [B, N, H, d] is {N*H*d, d, H*d}.
+ *   LSE stays [B, H, N] contiguous.  Everything else as fa_attn_fwd.
+ * Errors: as fa_attn_fwd, plus FA_ERR_INVALID_ARG for a NULL stride array and
+ * FA_ERR_MISALIGNED for a stride that breaks the 16-byte rule.
+ */
+int fa_attn_fwd_strided(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                        int B, int H, int N, int M, int d,
+                        const long long* q_stride, const long long* k_stride,
+                        const long long* v_stride, const long long* o_stride,
+                        float scale, int causal, int in_dtype, int out_dtype, void* stream);
 
 /*
  * fa_attn_fwd_splitkv -- fa_attn_fwd with the key tiles of each 256-row query

@@ -23,10 +23,15 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kRows = 64;  // query rows per CTA
 constexpr int kKeys = 32;  // keys per shared-memory tile
 
+struct StridesF32 {
+    long long q[3], k[3], v[3], o[3];  // element strides (batch, head, row)
+};
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kRows * (D >= 32 ? D / 32 : 1))
 attn_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K, const float* __restrict__ V,
-                float* __restrict__ O, float* __restrict__ LSE, int N, int M, float qscale) {
+                float* __restrict__ O, float* __restrict__ LSE, int N, int M, float qscale, int H, int coff,
+                StridesF32 st) {
     constexpr int G = D >= 32 ? D / 32 : 1;  // threads per row
     constexpr int C = D / G;                 // columns per thread
     constexpr int T = kRows * G;
@@ -37,10 +42,11 @@ attn_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K, const 
     const int g = tid % G;
     const int r = tid / G;
     const long bh = blockIdx.y;
+    const long hh = bh % H, bb = bh / H;
     const int i = blockIdx.x * kRows + r;  // query index
     const bool row_ok = i < N;
 
-    const float* q_row = Q + (bh * N + (row_ok ? i : 0)) * D;
+    const float* q_row = Q + bb * st.q[0] + hh * st.q[1] + (long)(row_ok ? i : 0) * st.q[2];
     float q[C], o[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) {
@@ -49,20 +55,21 @@ attn_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K, const 
     }
     float m = -CUDART_INF_F, l = 0.f;
 
-    const float* Kh = K + bh * (long)M * D;
-    const float* Vh = V + bh * (long)M * D;
+    const float* Kh = K + bb * st.k[0] + hh * st.k[1];
+    const float* Vh = V + bb * st.v[0] + hh * st.v[1];
     int kv_end = M;
     if (CAUSAL) {
+        // keys kept for query i: j <= i + coff (coff = 0 top-left, M - N bottom-right)
         const int last = min(N, (int)(blockIdx.x + 1) * kRows) - 1;  // last query row of this CTA
-        kv_end = min(M, last + 1);
+        kv_end = (int)max(0L, min((long)M, (long)last + coff + 1));
     }
     for (int k0 = 0; k0 < kv_end; k0 += kKeys) {
         __syncthreads();
         for (int e = tid; e < kKeys * D; e += T) {
             const int kk = e / D, c = e % D;
             const bool ok = k0 + kk < M;
-            Ks[kk][c] = ok ? Kh[(long)(k0 + kk) * D + c] : 0.f;
-            Vs[kk][c] = ok ? Vh[(long)(k0 + kk) * D + c] : 0.f;
+            Ks[kk][c] = ok ? Kh[(long)(k0 + kk) * st.k[2] + c] : 0.f;
+            Vs[kk][c] = ok ? Vh[(long)(k0 + kk) * st.v[2] + c] : 0.f;
         }
         __syncthreads();
         float x[kKeys];
@@ -75,7 +82,7 @@ attn_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K, const 
 #pragma unroll
             for (int off = 1; off < G; off <<= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
             const int key = k0 + kk;
-            const bool keep = key < M && (!CAUSAL || key <= i);
+            const bool keep = key < M && (!CAUSAL || key <= i + coff);
             x[kk] = keep ? part : -CUDART_INF_F;
             tmax = fmaxf(tmax, x[kk]);
         }
@@ -95,11 +102,12 @@ attn_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K, const 
         m = m_new;
     }
     if (!row_ok) return;
-    const float inv_l = 1.f / l;
-    float* o_row = O + (bh * N + i) * D;
+    // l = 0 only for a query with no kept key: O = 0, LSE = -inf
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    float* o_row = O + bb * st.o[0] + hh * st.o[1] + (long)i * st.o[2];
 #pragma unroll
     for (int c = 0; c < C; ++c) o_row[c * G + g] = o[c] * inv_l;
-    if (LSE != nullptr && g == 0) LSE[bh * N + i] = (m + __log2f(l)) * kLn2;
+    if (LSE != nullptr && g == 0) LSE[bh * N + i] = l > 0.f ? (m + __log2f(l)) * kLn2 : -CUDART_INF_F;
 }
 
 template <int D>
@@ -107,14 +115,19 @@ cudaError_t launch_d(const AttnParams& p, cudaStream_t st) {
     constexpr int G = D >= 32 ? D / 32 : 1;
     const dim3 grid((p.N + kRows - 1) / kRows, p.B * p.H);
     const float qscale = p.scale * kLog2e;
+    const int coff = p.causal == 2 ? p.M - p.N : 0;
+    StridesF32 s;
+    for (int i = 0; i < 3; ++i) {
+        s.q[i] = p.qs[i]; s.k[i] = p.ks[i]; s.v[i] = p.vs[i]; s.o[i] = p.os[i];
+    }
     if (p.causal)
         attn_f32_kernel<D, true><<<grid, kRows * G, 0, st>>>((const float*)p.Q, (const float*)p.K,
                                                             (const float*)p.V, (float*)p.O, p.LSE, p.N, p.M,
-                                                            qscale);
+                                                            qscale, p.H, coff, s);
     else
         attn_f32_kernel<D, false><<<grid, kRows * G, 0, st>>>((const float*)p.Q, (const float*)p.K,
                                                              (const float*)p.V, (float*)p.O, p.LSE, p.N, p.M,
-                                                             qscale);
+                                                             qscale, p.H, coff, s);
     return cudaGetLastError();
 }
 

@@ -23,7 +23,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D>
 __global__ void __launch_bounds__(kRowsPerBlock * 32)
 attn_combine_kernel(const float* __restrict__ Opart, const float* __restrict__ Lpart, void* __restrict__ O,
-                    float* __restrict__ LSE, long rows, int S, int out_bf16) {
+                    float* __restrict__ LSE, long rows, int S, int out_bf16, int N, int H, long long osb,
+                    long long osh, long long osr) {
     constexpr int C = D / 32;  // columns per lane
     const int lane = threadIdx.x & 31;
     const long row = (long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
@@ -40,7 +41,8 @@ attn_combine_kernel(const float* __restrict__ Opart, const float* __restrict__ L
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-    const float lse = mx + logf(sum);
+    // every split empty (a query with no kept key): O = 0, LSE = -inf
+    const float lse = sum > 0.f ? mx + logf(sum) : -CUDART_INF_F;
     float acc[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) acc[c] = 0.f;
@@ -52,12 +54,14 @@ attn_combine_kernel(const float* __restrict__ Opart, const float* __restrict__ L
 #pragma unroll
         for (int c = 0; c < C; ++c) acc[c] = fmaf(w, o[lane + 32 * c], acc[c]);
     }
+    const long bh = row / N, qi = row % N;
+    const long obase = (bh / H) * osb + (bh % H) * osh + qi * osr;
     if (out_bf16) {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(O) + row * D;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(O) + obase;
 #pragma unroll
         for (int c = 0; c < C; ++c) dst[lane + 32 * c] = __float2bfloat16_rn(acc[c]);
     } else {
-        float* dst = reinterpret_cast<float*>(O) + row * D;
+        float* dst = reinterpret_cast<float*>(O) + obase;
 #pragma unroll
         for (int c = 0; c < C; ++c) dst[lane + 32 * c] = acc[c];
     }
@@ -71,10 +75,12 @@ cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t st) {
     const dim3 grid((unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock));
     if (p.d == 64)
         attn_combine_kernel<64><<<grid, kRowsPerBlock * 32, 0, st>>>(p.Opart, p.Lpart, p.O, p.LSE, rows,
-                                                                    p.num_splits, p.out_bf16);
+                                                                    p.num_splits, p.out_bf16, p.N, p.H, p.os[0],
+                                                                    p.os[1], p.os[2]);
     else if (p.d == 128)
         attn_combine_kernel<128><<<grid, kRowsPerBlock * 32, 0, st>>>(p.Opart, p.Lpart, p.O, p.LSE, rows,
-                                                                     p.num_splits, p.out_bf16);
+                                                                     p.num_splits, p.out_bf16, p.N, p.H, p.os[0],
+                                                                     p.os[1], p.os[2]);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

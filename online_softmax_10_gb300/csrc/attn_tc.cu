@@ -89,14 +89,17 @@ static_assert(Cfg<128>::kSmemBytes <= 227 * 1024, "smem budget (d=128)");
 static_assert(Cfg<64>::kSmemBytes <= 227 * 1024, "smem budget (d=64)");
 
 // Number of key tiles Q tile t of the CTA starting at query row q0 must visit.
+// Under the causal mask key j is kept for query i iff j <= i + coff (coff = 0:
+// top-left, coff = M - N: bottom-right); a tile whose rows keep no key visits 0.
 template <bool CAUSAL>
-__device__ __forceinline__ int kv_tiles_for(int q0, int t, int N, int M) {
+__device__ __forceinline__ int kv_tiles_for(int q0, int t, int N, int M, int coff) {
     const int first = q0 + t * BM;
     if (first >= N) return 0;
     const int nM = (M + BN - 1) / BN;
     if (!CAUSAL) return nM;
-    const int last = min(N, first + BM) - 1;
-    return min(nM, last / BN + 1);
+    const long last_key = (long)(min(N, first + BM) - 1) + coff;
+    if (last_key < 0) return 0;
+    return (int)min((long)nM, last_key / BN + 1);
 }
 
 __device__ __forceinline__ void record_failure(volatile int* abort_flag, int* status) {
@@ -109,7 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, void* __restrict__ O, float* __restrict__ LSE,
                     int N, int M, float c_log2, int out_bf16, int* status, int nqb, int BH, int G, int S,
-                    float* __restrict__ Opart, float* __restrict__ Lpart) {
+                    float* __restrict__ Opart, float* __restrict__ Lpart, int H, int coff, long long osb,
+                    long long osh, long long osr) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -131,11 +135,12 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const long bh = g0 + r % gh;
     const int qblk = nqb - 1 - r / gh;
     const int q0 = qblk * 2 * BM;
+    const int hh = (int)(bh % H), bb = (int)(bh / H);  // head, batch (tensor-map coordinates)
     // This CTA covers key tiles [jb, jb + nk) of the ones its query block
     // needs (all of them when S = 1); n0, n1 count the tiles of that range each
     // Q tile uses, and j below runs over the range (key tile jb + j).
-    const int f0 = kv_tiles_for<CAUSAL>(q0, 0, N, M);
-    const int f1 = kv_tiles_for<CAUSAL>(q0, 1, N, M);
+    const int f0 = kv_tiles_for<CAUSAL>(q0, 0, N, M, coff);
+    const int f1 = kv_tiles_for<CAUSAL>(q0, 1, N, M, coff);
     const int fk = max(f0, f1);
     const int jb = (int)((long)split * fk / S);
     const int je = (int)((long)(split + 1) * fk / S);
@@ -175,8 +180,8 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if ((t == 0 ? n0 : n1) == 0) continue;
                 mbar_expect_tx(bar(C::QF(t)), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_3d_hint(base + C::kQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar(C::QF(t)),
-                                     a * 64, q0 + t * BM, (int)bh, pol_q);
+                    tma_load_4d_hint(base + C::kQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar(C::QF(t)),
+                                     a * 64, q0 + t * BM, hh, bb, pol_q);
             }
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < nk; ++j) {
@@ -188,8 +193,8 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 mbar_expect_tx(bar(C::KF(s)), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_3d(base + C::kK + s * C::kTileBytes + a * kAtomBytes, &tmK, bar(C::KF(s)),
-                                a * 64, (jb + j) * BN, (int)bh);
+                    tma_load_4d(base + C::kK + s * C::kTileBytes + a * kAtomBytes, &tmK, bar(C::KF(s)),
+                                a * 64, (jb + j) * BN, hh, bb);
                 issued_k = j + 1;
                 if (!mbar_wait_bounded(bar(C::VE(s)), ph ^ 1u, abort_flag, kWaitLimitNs)) {
                     record_failure(abort_flag, status);
@@ -197,8 +202,8 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 mbar_expect_tx(bar(C::VF(s)), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_3d(base + C::kV + s * C::kTileBytes + a * kAtomBytes, &tmV, bar(C::VF(s)),
-                                a * 64, (jb + j) * BN, (int)bh);
+                    tma_load_4d(base + C::kV + s * C::kTileBytes + a * kAtomBytes, &tmV, bar(C::VF(s)),
+                                a * 64, (jb + j) * BN, hh, bb);
                 issued_v = j + 1;
             }
             // Drain: the last copy issued into each stage has landed before the
@@ -308,12 +313,12 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 #pragma unroll
             for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
             const int k0 = (jb + j) * BN;
-            const bool need_mask = (k0 + BN > M) || (CAUSAL && k0 + BN - 1 > q0 + t * BM);
+            const bool need_mask = (k0 + BN > M) || (CAUSAL && k0 + BN - 1 > q0 + t * BM + coff);
             if (need_mask) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     const int key = k0 + c;
-                    if (key >= M || (CAUSAL && key > qi)) sv[c] = -CUDART_INF_F;
+                    if (key >= M || (CAUSAL && key > qi + coff)) sv[c] = -CUDART_INF_F;
                 }
             }
             // row max: three-input max over four independent chains
@@ -373,18 +378,29 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_arrive(bar(C::PF(t)));
         }
         // ------------------------------------------------------ epilogue
-        const long orow = bh * (long)N + qi;
+        const long orow = bh * (long)N + qi;                       // LSE / partial index
+        const long obase = bb * osb + hh * osh + (long)qi * osr;   // O element offset (strided)
         const bool store = qi < N;
-        if (S > 1 && n == 0 && ok && store) {
-            // no key of this split is kept for this row: an empty partial
-            Lpart[(long)split * BH * N + orow] = -CUDART_INF_F;
+        if (n == 0 && ok && store) {
+            // no key of this range is kept for this row
+            if (S > 1) {
+                Lpart[(long)split * BH * N + orow] = -CUDART_INF_F;  // an empty partial
+            } else {
+                // a query with no kept key at all (bottom-right mask, N > M): O = 0, LSE = -inf
+                for (int c = 0; c < D; ++c) {
+                    if (out_bf16) reinterpret_cast<__nv_bfloat16*>(O)[obase + c] = __float2bfloat16_rn(0.f);
+                    else reinterpret_cast<float*>(O)[obase + c] = 0.f;
+                }
+                if (LSE != nullptr) LSE[orow] = -CUDART_INF_F;
+            }
         }
         if (n > 0 && ok) {
             ok = mbar_wait_bounded(bar(C::OD(t)), 0, abort_flag, kWaitLimitNs);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (ok) {
                 tc_fence_after();
-                const float inv_l = 1.f / l;
+                // l = 0 only for a row with no kept key in this range: O = 0, LSE = -inf
+                const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t r[32];
@@ -399,7 +415,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                                                  __uint_as_float(r[4 * v + 2]) * inv_l,
                                                  __uint_as_float(r[4 * v + 3]) * inv_l);
                     } else if (out_bf16) {
-                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(O) + orow * D + ch * 32);
+                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(O) + obase + ch * 32);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint32_t w[4];
@@ -410,7 +426,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     } else {
-                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(O) + orow * D + ch * 32);
+                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(O) + obase + ch * 32);
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
                             dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
@@ -419,7 +435,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     }
                 }
                 if (store) {
-                    const float lse = (m + __log2f(l)) * kLn2;
+                    const float lse = l > 0.f ? (m + __log2f(l)) * kLn2 : -CUDART_INF_F;
                     if (S > 1) Lpart[(long)split * BH * N + orow] = lse;
                     else if (LSE != nullptr) LSE[orow] = lse;
                 }
@@ -468,8 +484,10 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtenso
     const int S = p.num_splits > 1 ? p.num_splits : 1;
     const dim3 grid((unsigned)((long)nqb * BH * S));
     const float c_log2 = p.scale * 1.4426950408889634f;
+    const int coff = p.causal == 2 ? p.M - p.N : 0;
     kern<<<grid, kThreads, Cf::kSmemBytes, st>>>(*tmQ, *tmK, *tmV, p.O, p.LSE, p.N, p.M, c_log2, p.out_bf16, p.status,
-                                                 nqb, BH, G, S, p.Opart, p.Lpart);
+                                                 nqb, BH, G, S, p.Opart, p.Lpart, p.H, coff, p.os[0], p.os[1],
+                                                 p.os[2]);
     return cudaGetLastError();
 }
 

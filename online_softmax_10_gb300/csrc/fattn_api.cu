@@ -74,16 +74,17 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [bh, rows, d] bf16 tensor -> 3-D tensor map, box 64 (d) x 128 (rows) x 1,
-// 128-byte swizzle, zero fill outside the tensor (ragged row tails).
-bool encode_bf16_3d(CUtensorMap* map, const void* ptr, long bh, long rows, int d) {
+// [B, H, rows, d] bf16 tensor with element strides (batch, head, row) and d
+// contiguous -> 4-D tensor map {d, rows, H, B}, box 64 (d) x 128 (rows) x 1 x 1,
+// 128-byte swizzle, zero fill past the last row (ragged row tails).
+bool encode_bf16_4d(CUtensorMap* map, const void* ptr, long B, long H, long rows, int d, const long long* st) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
+    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -104,7 +105,7 @@ int check_attn_args(const void* Q, const void* K, const void* V, void* O, float*
     if (!Q || !K || !V || !O) return FA_ERR_INVALID_ARG;
     if (B <= 0 || H <= 0 || N <= 0 || M <= 0 || d <= 0) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (causal < 0 || causal > 2) return FA_ERR_INVALID_ARG;
     const long kLim = 1L << 62;
     const long bh = (long)B * H;
     if (!mul_fits(bh, (long)(N > M ? N : M), kLim) || !mul_fits(bh * (N > M ? N : M), d, kLim / 4))
@@ -124,6 +125,52 @@ int check_attn_args(const void* Q, const void* K, const void* V, void* O, float*
 }
 
 constexpr int kMaxSplits = 64;
+
+struct Strides {
+    long long q[3], k[3], v[3], o[3];  // element strides (batch, head, row)
+};
+
+Strides contiguous_strides(int H, int N, int M, int d) {
+    Strides s;
+    const long long qn = (long long)N * d, km = (long long)M * d;
+    s.q[0] = s.o[0] = H * qn; s.q[1] = s.o[1] = qn; s.q[2] = s.o[2] = d;
+    s.k[0] = s.v[0] = H * km; s.k[1] = s.v[1] = km; s.k[2] = s.v[2] = d;
+    return s;
+}
+
+// Element strides that are positive and whole multiples of 16 bytes.
+bool strides_ok(const long long* st, int esize) {
+    for (int i = 0; i < 3; ++i)
+        if (st[i] <= 0 || (st[i] * esize) % 16 != 0 || st[i] > (1LL << 40)) return false;
+    return true;
+}
+
+// Launch the attention kernel(s) for validated arguments.
+int attn_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int M, int d,
+                const Strides& st, float scale, int causal, int S, float* opart, float* lpart, int in_dtype,
+                int out_dtype, void* stream) {
+    int err = FA_OK;
+    int* status = status_word(&err);
+    if (status == nullptr) return err;
+    fa::AttnParams p{Q,      K, V,     O,     LSE, B, H, N, M, d, scale, causal, out_dtype == FA_BF16 ? 1 : 0,
+                     status, S, opart, lpart, {},  {}, {}, {}};
+    for (int i = 0; i < 3; ++i) {
+        p.qs[i] = st.q[i]; p.ks[i] = st.k[i]; p.vs[i] = st.v[i]; p.os[i] = st.o[i];
+    }
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (in_dtype == FA_F32) {
+        e = fa::launch_attn_f32(p, cs);
+    } else {
+        CUtensorMap tq, tk, tv;
+        if (!encode_bf16_4d(&tq, Q, B, H, N, d, st.q) || !encode_bf16_4d(&tk, K, B, H, M, d, st.k) ||
+            !encode_bf16_4d(&tv, V, B, H, M, d, st.v))
+            return FA_ERR_CUDA;
+        e = fa::launch_attn_bf16_tc(p, &tq, &tk, &tv, num_sms(), cs);
+        if (e == cudaSuccess && S > 1) e = fa::launch_attn_combine(p, cs);
+    }
+    return cuda_status(e);
+}
 
 // Bytes of split workspace: partial O (fp32) then partial LSE, 256-B aligned.
 long splitkv_bytes(long bh, long N, long d, long S, long* lse_offset) {
@@ -169,25 +216,27 @@ int fa_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE
                 float scale, int causal, int in_dtype, int out_dtype, void* stream) {
     const int chk = check_attn_args(Q, K, V, O, LSE, B, H, N, M, d, scale, causal, in_dtype, out_dtype);
     if (chk != FA_OK) return chk;
-    const long bh = (long)B * H;
+    return attn_launch(Q, K, V, O, LSE, B, H, N, M, d, contiguous_strides(H, N, M, d), scale, causal, 1, nullptr,
+                       nullptr, in_dtype, out_dtype, stream);
+}
 
-    int err = FA_OK;
-    int* status = status_word(&err);
-    if (status == nullptr) return err;
-    fa::AttnParams p{Q,     K,      V, O, LSE, B, H, N, M, d, scale, causal, out_dtype == FA_BF16 ? 1 : 0,
-                     status, 1,      nullptr, nullptr};
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (in_dtype == FA_F32) {
-        e = fa::launch_attn_f32(p, st);
-    } else {
-        CUtensorMap tq, tk, tv;
-        if (!encode_bf16_3d(&tq, Q, bh, N, d) || !encode_bf16_3d(&tk, K, bh, M, d) ||
-            !encode_bf16_3d(&tv, V, bh, M, d))
-            return FA_ERR_CUDA;
-        e = fa::launch_attn_bf16_tc(p, &tq, &tk, &tv, num_sms(), st);
+int fa_attn_fwd_strided(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int M,
+                        int d, const long long* q_stride, const long long* k_stride, const long long* v_stride,
+                        const long long* o_stride, float scale, int causal, int in_dtype, int out_dtype,
+                        void* stream) {
+    const int chk = check_attn_args(Q, K, V, O, LSE, B, H, N, M, d, scale, causal, in_dtype, out_dtype);
+    if (chk != FA_OK) return chk;
+    if (!q_stride || !k_stride || !v_stride || !o_stride) return FA_ERR_INVALID_ARG;
+    const int ie = in_dtype == FA_BF16 ? 2 : 4, oe = out_dtype == FA_BF16 ? 2 : 4;
+    if (!strides_ok(q_stride, ie) || !strides_ok(k_stride, ie) || !strides_ok(v_stride, ie) ||
+        !strides_ok(o_stride, oe))
+        return FA_ERR_MISALIGNED;
+    Strides st;
+    for (int i = 0; i < 3; ++i) {
+        st.q[i] = q_stride[i]; st.k[i] = k_stride[i]; st.v[i] = v_stride[i]; st.o[i] = o_stride[i];
     }
-    return cuda_status(e);
+    return attn_launch(Q, K, V, O, LSE, B, H, N, M, d, st, scale, causal, 1, nullptr, nullptr, in_dtype, out_dtype,
+                       stream);
 }
 
 int fa_attn_splitkv_num_splits(int B, int H, int N, int M, int d, int causal) {
@@ -217,20 +266,10 @@ int fa_attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, fl
     const long need = splitkv_bytes(bh, N, d, S, &loff);
     if (workspace == nullptr || workspace_bytes < need) return FA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_MISALIGNED;
-    int err = FA_OK;
-    int* status = status_word(&err);
-    if (status == nullptr) return err;
     float* opart = static_cast<float*>(workspace);
     float* lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + loff);
-    fa::AttnParams p{Q,      K, V, O, LSE, B, H, N, M, d, scale, causal, out_dtype == FA_BF16 ? 1 : 0,
-                     status, S, opart, lpart};
-    CUtensorMap tq, tk, tv;
-    if (!encode_bf16_3d(&tq, Q, bh, N, d) || !encode_bf16_3d(&tk, K, bh, M, d) || !encode_bf16_3d(&tv, V, bh, M, d))
-        return FA_ERR_CUDA;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = fa::launch_attn_bf16_tc(p, &tq, &tk, &tv, num_sms(), st);
-    if (e == cudaSuccess) e = fa::launch_attn_combine(p, st);
-    return cuda_status(e);
+    return attn_launch(Q, K, V, O, LSE, B, H, N, M, d, contiguous_strides(H, N, M, d), scale, causal, S, opart, lpart,
+                       in_dtype, out_dtype, stream);
 }
 
 namespace {

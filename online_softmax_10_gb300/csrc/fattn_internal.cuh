@@ -22,12 +22,13 @@ struct AttnParams {
     float* LSE;        // may be null
     int B, H, N, M, d;
     float scale;       // > 0
-    int causal;
+    int causal;        // 0 none, 1 top-left (j <= i), 2 bottom-right (j <= i + M - N)
     int out_bf16;      // 1: O is bf16, 0: O is fp32
     int* status;       // device status word
     int num_splits;    // > 1: key tiles split over this many CTAs (bf16 path only)
     float* Opart;      // split partial outputs, fp32 [num_splits][B*H][N][d]
     float* Lpart;      // split partial LSE, fp32 [num_splits][B*H][N]
+    long long qs[3], ks[3], vs[3], os[3];  // element strides (batch, head, row); d is contiguous
 };
 
 // Row-wise kernels (softmax_rows.cu).
@@ -43,8 +44,8 @@ cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long col
 cudaError_t launch_attn_f32(const AttnParams& p, cudaStream_t stream);
 
 // bf16 tensor-core attention (attn_tc.cu).  d in {64, 128}.  The three tensor
-// maps describe Q [B*H, N, d], K and V [B*H, M, d] as 3-D bf16 tensors with
-// a 64 x 128 box and 128-byte swizzle.
+// maps describe Q [B, H, N, d], K and V [B, H, M, d] (any strides) as 4-D bf16
+// tensors {d, rows, H, B} with a 64 x 128 x 1 x 1 box and 128-byte swizzle.
 cudaError_t launch_attn_bf16_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                 const CUtensorMap* tmV, int num_sms, cudaStream_t stream);
 

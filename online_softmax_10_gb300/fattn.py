@@ -25,6 +25,8 @@ _c_int, _c_long, _c_float, _vp = ctypes.c_int, ctypes.c_long, ctypes.c_float, ct
 SIGNATURES = {
     "fa_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
                              _c_int, _c_int, _vp]),
+    "fa_attn_fwd_strided": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,
+                                     _vp, _c_float, _c_int, _c_int, _c_int, _vp]),
     "fa_attn_fwd_splitkv": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                      _c_int, _c_int, _vp, _c_long, _c_int, _c_int, _vp]),
     "fa_attn_fwd_splitkv_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
@@ -101,6 +103,16 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def causal_code(causal) -> int:
+    """False/0: no mask; True/1/'top_left': key j kept iff j <= i;
+    2/'bottom_right': iff j <= i + (M - N)."""
+    if causal in (2, "bottom_right"):
+        return 2
+    if causal in ("top_left",):
+        return 1
+    return int(bool(causal))
+
+
 def attn_fwd(q, k, v, scale: float | None = None, causal: bool = False, out_dtype=None, out=None, lse=None,
              want_lse: bool = True, stream=None):
     """O = softmax(scale * q k^T [+ causal]) v and LSE, through fa_attn_fwd.
@@ -122,14 +134,53 @@ def attn_fwd(q, k, v, scale: float | None = None, causal: bool = False, out_dtyp
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _check_cuda(out, *([lse] if lse is not None else []))
     rc = lib().fa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, M, d, float(scale),
-                           int(bool(causal)), _dtype_code(q.dtype), _dtype_code(out.dtype), _stream(stream))
+                           causal_code(causal), _dtype_code(q.dtype), _dtype_code(out.dtype), _stream(stream))
     if rc != FA_OK:
         raise FattnError(rc, "fa_attn_fwd")
     return out, lse
 
 
+def attn_fwd_strided(q, k, v, scale: float | None = None, causal=False, out=None, lse=None, want_lse: bool = True,
+                     layout: str = "bshd", stream=None):
+    """fa_attn_fwd_strided on views with any batch/head/row strides.
+
+    With layout="bshd", q is [B, N, H, d], k/v [B, M, H, d] and ``out`` (made
+    here if not given) is [B, N, H, d]; with layout="bhsd" the usual
+    [B, H, N, d].  Strides are taken from the tensors themselves (d must be
+    the contiguous dimension).  LSE is [B, H, N]."""
+    for t in (q, k, v):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.stride(-1) != 1:
+            raise ValueError("CUDA tensors with a contiguous last dimension are required")
+    if layout == "bshd":
+        B, N, H, d = q.shape
+        M = k.shape[1]
+        pick = lambda t: (t.stride(0), t.stride(2), t.stride(1))  # (batch, head, row)
+        oshape = (B, N, H, d)
+    elif layout == "bhsd":
+        B, H, N, d = q.shape
+        M = k.shape[2]
+        pick = lambda t: (t.stride(0), t.stride(1), t.stride(2))
+        oshape = (B, H, N, d)
+    else:
+        raise ValueError(layout)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(oshape, dtype=q.dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    arr = lambda t: (ctypes.c_longlong * 3)(*pick(t))
+    qs, ks, vs, os_ = arr(q), arr(k), arr(v), arr(out)
+    rc = lib().fa_attn_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, M, d, qs, ks, vs, os_,
+                                   float(scale), causal_code(causal), _dtype_code(q.dtype), _dtype_code(out.dtype),
+                                   _stream(stream))
+    if rc != FA_OK:
+        raise FattnError(rc, "fa_attn_fwd_strided")
+    return out, lse
+
+
 def splitkv_num_splits(B: int, H: int, N: int, M: int, d: int, causal: bool) -> int:
-    return lib().fa_attn_splitkv_num_splits(B, H, N, M, d, int(bool(causal)))
+    return lib().fa_attn_splitkv_num_splits(B, H, N, M, d, causal_code(causal))
 
 
 def splitkv_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int) -> int:
@@ -149,7 +200,7 @@ def attn_fwd_splitkv(q, k, v, scale: float | None = None, causal: bool = False, 
         raise ValueError("q, k, v shapes/dtypes do not match")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    S = num_splits if num_splits > 0 else splitkv_num_splits(B, H, N, M, d, causal)
+    S = num_splits if num_splits > 0 else splitkv_num_splits(B, H, N, M, d, causal_code(causal))
     need = splitkv_workspace_bytes(B, H, N, d, S)
     if need < 0:
         raise ValueError("invalid split count")
@@ -162,7 +213,7 @@ def attn_fwd_splitkv(q, k, v, scale: float | None = None, causal: bool = False, 
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib().fa_attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, M, d, float(scale),
-                                   int(bool(causal)), S, _ptr(workspace), wbytes, _dtype_code(q.dtype),
+                                   causal_code(causal), S, _ptr(workspace), wbytes, _dtype_code(q.dtype),
                                    _dtype_code(out.dtype), _stream(stream))
     if rc != FA_OK:
         raise FattnError(rc, "fa_attn_fwd_splitkv")
@@ -184,7 +235,7 @@ def attn_fwd_splitkv_noalloc(q, k, v, scale: float | None = None, causal: bool =
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     rc = lib().fa_attn_fwd_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, M, d,
-                                           float(scale), int(bool(causal)), int(num_splits), _dtype_code(q.dtype),
+                                           float(scale), causal_code(causal), int(num_splits), _dtype_code(q.dtype),
                                            _dtype_code(out.dtype), _stream(stream))
     if rc != FA_OK:
         raise FattnError(rc, "fa_attn_fwd_splitkv_noalloc")

@@ -61,7 +61,7 @@ def attn(L, Q=P, K=P, V=P, O=P, LSE=P, B=1, H=1, N=8, M=8, d=64, scale=0.125, ca
     (dict(Q=None), INVALID), (dict(K=None), INVALID), (dict(V=None), INVALID), (dict(O=None), INVALID),
     (dict(B=0), INVALID), (dict(H=-1), INVALID), (dict(N=0), INVALID), (dict(M=0), INVALID), (dict(d=0), INVALID),
     (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID), (dict(scale=float("nan")), INVALID),
-    (dict(scale=float("inf")), INVALID), (dict(causal=2), INVALID),
+    (dict(scale=float("inf")), INVALID), (dict(causal=3), INVALID), (dict(causal=-1), INVALID),
     (dict(i=7), UNSUPPORTED), (dict(o=9), UNSUPPORTED), (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED),
     (dict(i=0, o=1), UNSUPPORTED), (dict(i=0, d=48), UNSUPPORTED), (dict(B=300, H=300), UNSUPPORTED),
     (dict(Q=P + 8), MISALIGNED), (dict(O=P + 2), MISALIGNED), (dict(LSE=P + 4), MISALIGNED),
@@ -137,3 +137,19 @@ def test_row_extras_argument_errors(L):
     assert L.fa_cross_entropy_rows(P, P, P, P, 0, 8, 1, None) == INVALID
     assert L.fa_cross_entropy_rows(P, P + 8, P, None, 4, 8, 1, None) == MISALIGNED
     assert L.fa_cross_entropy_rows(P, P, P, None, 4, 8, 3, None) == UNSUPPORTED
+
+
+def test_strided_argument_errors(L):
+    import ctypes
+    arr = lambda *v: (ctypes.c_longlong * 3)(*v)
+    good = arr(1 << 20, 64 * 8, 64 * 4)                   # bf16: multiples of 8 elements
+    f = L.fa_attn_fwd_strided
+    base = [P, P, P, P, P, 1, 4, 8, 8, 64]
+    assert f(*base, None, good, good, good, 0.1, 0, 1, 1, None) == INVALID
+    assert f(*base, good, good, good, None, 0.1, 0, 1, 1, None) == INVALID
+    assert f(*base, arr(1 << 20, 64 * 8, 60), good, good, good, 0.1, 0, 1, 1, None) == MISALIGNED  # 120 B rows
+    assert f(*base, good, arr(0, 64, 64), good, good, 0.1, 0, 1, 1, None) == MISALIGNED              # zero stride
+    assert f(*base, good, good, good, arr(1 << 20, 64 * 8, 66), 0.1, 0, 1, 1, None) == MISALIGNED
+    assert f(*base, good, good, good, good, 0.1, 3, 1, 1, None) == INVALID                           # causal mode
+    # fp32 needs 16-byte strides too: 4 elements
+    assert f(*[P, P, P, P, P, 1, 4, 8, 8, 64], arr(4096, 512, 66), good, good, good, 0.1, 0, 0, 0, None) == MISALIGNED

@@ -149,3 +149,68 @@ def test_bf16_side_stream_and_no_lse():
     s.synchronize()
     assert lse is None
     assert torch.equal(o, ref)
+
+
+# ----------------------------------------------------------------- bottom-right causal
+BR_SHAPES = [(300, 100), (100, 300), (257, 1000), (1000, 257), (1, 300), (300, 1), (129, 129)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N,M", BR_SHAPES)
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_bf16_bottom_right_causal(d, N, M, out):
+    # key j kept for query i iff j <= i + (M - N); with N > M the first N - M
+    # queries keep no key and must come back as O = 0, LSE = -inf
+    q, k, v = inputs.attn_inputs(1, 2, N, M, d, torch.bfloat16, seed=N * 3 + M + d)
+    err, ratio, ok, rel = attn_case(q, k, v, 2, out_dtype=torch.float32 if out == "f32" else None)
+    assert ratio <= 1.0, err
+    assert ok, rel
+
+
+@pytest.mark.parametrize("d", [16, 64, 128])
+@pytest.mark.parametrize("N,M", [(70, 130), (130, 70), (1, 40), (40, 1)])
+def test_f32_bottom_right_causal(d, N, M):
+    q, k, v = inputs.attn_inputs(2, 2, N, M, d, torch.float32, seed=N + M + d)
+    err, ratio, ok, rel = attn_case(q, k, v, 2)
+    assert ratio <= 1.0, err
+    assert ok, rel
+
+
+# ----------------------------------------------------------------- strided layouts
+def _oracle_check(q, k, v, causal, o, lse, o_tol_rel=None):
+    import oracle
+    d = q.shape[-1]
+    O_ref, L_ref = oracle.attn_fwd(q, k, v, 1.0 / math.sqrt(d), causal)
+    og = o.float().cpu().double().numpy()
+    tol = (1e-5 if q.dtype == torch.float32 else 1e-2) + (2.0 ** -8 * np.abs(O_ref) if o.dtype == torch.bfloat16 else 0)
+    assert np.all(np.abs(og - O_ref) <= tol), float(np.max(np.abs(og - O_ref)))
+    from parity import lse_ok
+    ok, rel = lse_ok(lse.cpu().double().numpy(), L_ref)
+    assert ok, rel
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 64), (torch.bfloat16, 128), (torch.float32, 64)])
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_strided_bshd_layout(dtype, d, causal):
+    B, H, N, M = 2, 3, 300, 520
+    q, k, v = inputs.attn_inputs(B, H, N, M, d, dtype, seed=d + causal)
+    # the same values laid out [B, N, H, d]
+    qs, ks, vs = (t.permute(0, 2, 1, 3).contiguous().cuda() for t in (q, k, v))
+    o, lse = fattn.attn_fwd_strided(qs, ks, vs, causal=causal, layout="bshd")
+    assert fattn.device_status() == fattn.FA_OK
+    assert o.shape == (B, N, H, d)
+    _oracle_check(q, k, v, causal, o.permute(0, 2, 1, 3), lse)
+
+
+def test_strided_padded_rows_bf16():
+    # [B, H, N, d] views cut out of wider rows (row stride 2d) and an output
+    # with a padded row stride as well
+    B, H, N, M, d = 1, 2, 200, 333, 128
+    q, k, v = inputs.attn_inputs(B, H, N, M, d, torch.bfloat16, seed=8)
+    wide = lambda t: torch.cat([t, torch.zeros_like(t)], -1).cuda()[..., :d]
+    qw, kw, vw = wide(q), wide(k), wide(v)
+    ow = torch.zeros(B, H, N, 2 * d, dtype=torch.bfloat16, device="cuda")[..., :d]
+    o, lse = fattn.attn_fwd_strided(qw, kw, vw, causal=1, out=ow, layout="bhsd")
+    assert fattn.device_status() == fattn.FA_OK
+    _oracle_check(q, k, v, 1, o, lse)
+    assert torch.all(ow.as_strided((B, H, N, d), (H * N * 2 * d, N * 2 * d, 2 * d, 1), d) == 0)  # padding untouched

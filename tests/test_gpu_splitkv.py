@@ -37,7 +37,7 @@ def _split_case(q, k, v, causal, splits, out_dtype=None, rows=None):
 @pytest.mark.parametrize("splits", [2, 3, 7, 16, 0])
 @pytest.mark.parametrize("B,H,N,M,d,causal", [
     (1, 2, 300, 2100, 128, False), (1, 2, 300, 2100, 64, True), (2, 1, 129, 1000, 128, True),
-    (1, 3, 64, 8192, 128, False), (1, 2, 1000, 1000, 64, True)])
+    (1, 3, 64, 8192, 128, False), (1, 2, 1000, 1000, 64, True), (1, 2, 300, 2100, 128, 2), (1, 2, 2100, 300, 64, 2)])
 def test_splitkv_matches_oracle(splits, B, H, N, M, d, causal):
     q, k, v = inputs.attn_inputs(B, H, N, M, d, torch.bfloat16, seed=N + M + splits)
     for out in (None, torch.float32):
