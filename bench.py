@@ -293,26 +293,51 @@ def run_ours(args, world_size, rank, local_rank):
     value = aggregate_throughput(flops, world_size, total_s / args.steps) / 1e12
     achieved = flops / per_launch_s / 1e12
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step
+    # copies its Q, K, V in from pinned host memory and its O, LSE back out.
+    # Two device input sets let step i+1's upload (copy stream) overlap step
+    # i's kernel and download (compute stream); events order the hand-offs.
     qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
     op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dev_in = [tuple(torch.empty_like(t) for t in (q, k, v)) for _ in range(2)]
+    copy_stream = torch.cuda.Stream()
+    comp = torch.cuda.current_stream()
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    for ev in consumed:
+        ev.record(comp)
+
+    def upload(slot):
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(consumed[slot])
+            for dst, src in zip(dev_in[slot], (qp, kp, vp)):
+                dst.copy_(src, non_blocking=True)
+            uploaded[slot].record(copy_stream)
+
+    e2e_state = {"i": 0}
 
     def e2e_step():
-        qd.copy_(qp, non_blocking=True)
-        kd.copy_(kp, non_blocking=True)
-        vd.copy_(vp, non_blocking=True)
+        i = e2e_state["i"]
+        slot = i % 2
+        if i == 0:
+            upload(0)
+        upload(1 - slot)  # the next step's inputs, while this step computes
+        comp.wait_event(uploaded[slot])
+        qd, kd, vd = dev_in[slot]
         fattn.attn_fwd(qd, kd, vd, w.scale, w.causal, out=o, lse=lse)
+        consumed[slot].record(comp)
         op.copy_(o, non_blocking=True)
         lp.copy_(lse, non_blocking=True)
+        e2e_state["i"] = i + 1
 
     e2e_steps = max(3, min(args.steps, 30))
     e2e_total, _ = time_launches(e2e_step, e2e_steps, 2, world_size)
+    torch.cuda.synchronize()
     e2e_value = aggregate_throughput(flops, world_size, e2e_total / e2e_steps) / 1e12
     h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
-    del qd, kd, vd, qp, kp, vp
+    del dev_in, qp, kp, vp
 
     # ---- row softmax workload (second headline): bf16 [4096, 32768] -> bf16 P + fp32 LSE
     rw = inputs.ROWS_4096x32768
@@ -370,7 +395,8 @@ def run_ours(args, world_size, rank, local_rank):
                      "algorithmic_bytes": alg_bytes,
                      "peak_source": f"bf16_tflops (burst), {peak_src}"},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "pipelining": "step i+1's host-to-device copy overlaps step i's kernel and device-to-host copy"},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "row_softmax": {"workload": rw.name, "value": r_gbs, "unit": "GB/s", "us_per_launch": r_per * 1e6,

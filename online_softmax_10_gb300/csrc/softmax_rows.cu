@@ -570,6 +570,7 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
         // to the producer as soon as the second half is in registers
         const TIn* srow = reinterpret_cast<const TIn*>(gbase + (uint32_t)s * stage_bytes);
         constexpr int NH = NV / 2;
+        const bool whole_slice = (long)NV * kLseGroupThreads <= nvec;
         float m = -CUDART_INF_F, sum = 0.f;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -588,7 +589,8 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
                 float v[CH][V];
 #pragma unroll
                 for (int kk = 0; kk < CH; ++kk) {
-                    const bool in = gt + (long)(half * NH + k0 + kk) * kLseGroupThreads < nvec;
+                    // (whole_slice: every vector of this thread is in the row; no per-element select)
+                    const bool in = whole_slice || gt + (long)(half * NH + k0 + kk) * kLseGroupThreads < nvec;
                     const uint4 u = raw[k0 + kk];
                     if constexpr (V == 8) {
                         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
