@@ -62,25 +62,28 @@ template <int D>
 struct Cfg {
     static constexpr int kAtoms = D / 64;                        // 128-byte column blocks per row
     static constexpr uint32_t kTileBytes = (uint32_t)BM * D * 2; // one 128-row bf16 tile
-    static constexpr int NST = D == 128 ? 2 : 4;                 // K/V ring depth
+    // Ring depths.  A V tile is released only after the second Q tile's P V,
+    // one key step later than its K tile, so V gets one stage more.
+    static constexpr int NSTK = D == 128 ? 2 : 4;                // K ring depth
+    static constexpr int NSTV = D == 128 ? 3 : 5;                // V ring depth
     static constexpr uint32_t kQ = 0;                            // Q_0, Q_1
     static constexpr uint32_t kK = 2 * kTileBytes;               // K ring
-    static constexpr uint32_t kV = kK + NST * kTileBytes;        // V ring
-    static constexpr uint32_t kBar = kV + NST * kTileBytes;      // mbarriers
-    static constexpr int kNumBars = 9 + 4 * NST;
+    static constexpr uint32_t kV = kK + NSTK * kTileBytes;       // V ring
+    static constexpr uint32_t kBar = kV + NSTV * kTileBytes;     // mbarriers
+    static constexpr int kNumBars = 9 + 2 * NSTK + 2 * NSTV;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kSmemBytes = kAbort + 4 + 1024;    // + slack to align the base
     // barrier indices
     __host__ __device__ static constexpr int QF(int t) { return t; }
     __host__ __device__ static constexpr int KF(int s) { return 2 + s; }
-    __host__ __device__ static constexpr int KE(int s) { return 2 + NST + s; }
-    __host__ __device__ static constexpr int VF(int s) { return 2 + 2 * NST + s; }
-    __host__ __device__ static constexpr int VE(int s) { return 2 + 3 * NST + s; }
-    __host__ __device__ static constexpr int SF(int t) { return 2 + 4 * NST + t; }
-    __host__ __device__ static constexpr int PF(int t) { return 4 + 4 * NST + t; }
-    __host__ __device__ static constexpr int OD(int t) { return 6 + 4 * NST + t; }
-    static constexpr int DRAIN = 8 + 4 * NST;
+    __host__ __device__ static constexpr int KE(int s) { return 2 + NSTK + s; }
+    __host__ __device__ static constexpr int VF(int s) { return 2 + 2 * NSTK + s; }
+    __host__ __device__ static constexpr int VE(int s) { return 2 + 2 * NSTK + NSTV + s; }
+    __host__ __device__ static constexpr int SF(int t) { return 2 + 2 * NSTK + 2 * NSTV + t; }
+    __host__ __device__ static constexpr int PF(int t) { return 4 + 2 * NSTK + 2 * NSTV + t; }
+    __host__ __device__ static constexpr int OD(int t) { return 6 + 2 * NSTK + 2 * NSTV + t; }
+    static constexpr int DRAIN = 8 + 2 * NSTK + 2 * NSTV;
     // tensor-memory columns
     __host__ __device__ static constexpr uint32_t colS(int t) { return (uint32_t)t * 128u; }
     __host__ __device__ static constexpr uint32_t colO(int t) { return 256u + (uint32_t)t * D; }
@@ -185,8 +188,8 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < nk; ++j) {
-                const int s = j % C::NST;
-                const uint32_t ph = (uint32_t)(j / C::NST) & 1u;
+                const int s = j % C::NSTK, sv = j % C::NSTV;
+                const uint32_t ph = (uint32_t)(j / C::NSTK) & 1u, phv = (uint32_t)(j / C::NSTV) & 1u;
                 if (!mbar_wait_bounded(bar(C::KE(s)), ph ^ 1u, abort_flag, kWaitLimitNs)) {
                     record_failure(abort_flag, status);
                     break;
@@ -196,23 +199,23 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     tma_load_4d(base + C::kK + s * C::kTileBytes + a * kAtomBytes, &tmK, bar(C::KF(s)),
                                 a * 64, (jb + j) * BN, hh, bb);
                 issued_k = j + 1;
-                if (!mbar_wait_bounded(bar(C::VE(s)), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                if (!mbar_wait_bounded(bar(C::VE(sv)), phv ^ 1u, abort_flag, kWaitLimitNs)) {
                     record_failure(abort_flag, status);
                     break;
                 }
-                mbar_expect_tx(bar(C::VF(s)), C::kTileBytes);
+                mbar_expect_tx(bar(C::VF(sv)), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_4d(base + C::kV + s * C::kTileBytes + a * kAtomBytes, &tmV, bar(C::VF(s)),
+                    tma_load_4d(base + C::kV + sv * C::kTileBytes + a * kAtomBytes, &tmV, bar(C::VF(sv)),
                                 a * 64, (jb + j) * BN, hh, bb);
                 issued_v = j + 1;
             }
             // Drain: the last copy issued into each stage has landed before the
             // CTA may exit (returns at once on the normal path, where every
             // copy has been consumed).
-            for (int j = max(0, issued_k - C::NST); j < issued_k; ++j)
-                mbar_wait_bounded(bar(C::KF(j % C::NST)), (uint32_t)(j / C::NST) & 1u, nullptr, kWaitLimitNs);
-            for (int j = max(0, issued_v - C::NST); j < issued_v; ++j)
-                mbar_wait_bounded(bar(C::VF(j % C::NST)), (uint32_t)(j / C::NST) & 1u, nullptr, kWaitLimitNs);
+            for (int j = max(0, issued_k - C::NSTK); j < issued_k; ++j)
+                mbar_wait_bounded(bar(C::KF(j % C::NSTK)), (uint32_t)(j / C::NSTK) & 1u, nullptr, kWaitLimitNs);
+            for (int j = max(0, issued_v - C::NSTV); j < issued_v; ++j)
+                mbar_wait_bounded(bar(C::VF(j % C::NSTV)), (uint32_t)(j / C::NSTV) & 1u, nullptr, kWaitLimitNs);
             for (int t = 0; t < 2; ++t)
                 if ((t == 0 ? n0 : n1) > 0) mbar_wait_bounded(bar(C::QF(t)), 0, nullptr, kWaitLimitNs);
         }
@@ -222,22 +225,29 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);    // P from TMEM, V MN-major
             const int nt[2] = {n0, n1};
+            // Issuing one tcgen05.mma takes this thread about as long as the
+            // tensor pipe needs to run a 128x128x16 one, so every instruction
+            // it spends between MMAs shows up as pipe idle time.  Descriptors
+            // are therefore built once: the start-address field (address / 16,
+            // 14 bits) of every operand block follows by adding its offset / 16
+            // (shared addresses stay below 256 KB, so the field cannot carry).
+            const uint64_t dQ = umma_desc_sw128(base + C::kQ, 16, 1024);
+            const uint64_t dK = umma_desc_sw128(base + C::kK, 16, 1024);
+            const uint64_t dV = umma_desc_sw128(base + C::kV, kAtomBytes, 1024);
             auto issue_S = [&](int t, int s) {
-                const uint32_t qa = base + C::kQ + t * C::kTileBytes;
-                const uint32_t kb = base + C::kK + s * C::kTileBytes;
+                const uint64_t qa = dQ + ((uint32_t)t * C::kTileBytes >> 4);
+                const uint64_t kb = dK + ((uint32_t)s * C::kTileBytes >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kAtomBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tmem + C::colS(t), umma_desc_sw128(qa + off, 16, 1024), umma_desc_sw128(kb + off, 16, 1024),
-                           idS, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((uint32_t)(kk >> 2) * kAtomBytes + (uint32_t)(kk & 3) * 32u) >> 4;
+                    mma_ss(tmem + C::colS(t), qa + off, kb + off, idS, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_PV = [&](int t, int s, bool acc) {
-                const uint32_t vb = base + C::kV + s * C::kTileBytes;
+                const uint64_t vb = dV + ((uint32_t)s * C::kTileBytes >> 4);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    mma_ts(tmem + C::colO(t), tmem + C::colS(t) + (uint32_t)kk * 8u,
-                           umma_desc_sw128(vb + (uint32_t)kk * 2048u, kAtomBytes, 1024), idO,
+                    mma_ts(tmem + C::colO(t), tmem + C::colS(t) + (uint32_t)kk * 8u, vb + ((uint32_t)kk * 2048u >> 4), idO,
                            (acc || kk > 0) ? 1u : 0u);
                 }
             };
@@ -256,14 +266,16 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 mma_commit(bar(C::KE(0)));
             }
             for (int j = 0; j < nk && ok; ++j) {
-                const int s = j % C::NST;
-                const uint32_t ph = (uint32_t)(j / C::NST) & 1u;
+                const int s = j % C::NSTV;
+                const uint32_t ph = (uint32_t)(j / C::NSTV) & 1u;
                 const int jn = j + 1;
-                const int sn = jn % C::NST;
-                const uint32_t phn = (uint32_t)(jn / C::NST) & 1u;
-                bool kn_ready = false;
+                const int sn = jn % C::NSTK;
+                const uint32_t phn = (uint32_t)(jn / C::NSTK) & 1u;
+                // Both operand tiles of this step are waited for up front, so a
+                // tile's P V and its next Q K^T go to the tensor pipe back to back.
+                const bool kn_ready = jn < nk;
                 if (!(ok = mbar_wait_bounded(bar(C::VF(s)), ph, abort_flag, kWaitLimitNs))) break;
-                tc_fence_after();
+                if (kn_ready && !(ok = mbar_wait_bounded(bar(C::KF(sn)), phn, abort_flag, kWaitLimitNs))) break;
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j >= nt[t]) continue;
                     if (!(ok = mbar_wait_bounded(bar(C::PF(t)), (uint32_t)j & 1u, abort_flag, kWaitLimitNs))) break;
@@ -271,11 +283,6 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     issue_PV(t, s, j > 0);
                     if (j == nt[t] - 1) mma_commit(bar(C::OD(t)));
                     if (jn < nt[t]) {
-                        if (!kn_ready) {
-                            if (!(ok = mbar_wait_bounded(bar(C::KF(sn)), phn, abort_flag, kWaitLimitNs))) break;
-                            tc_fence_after();
-                            kn_ready = true;
-                        }
                         issue_S(t, sn);
                         mma_commit(bar(C::SF(t)));
                     }
