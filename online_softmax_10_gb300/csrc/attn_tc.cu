@@ -21,7 +21,8 @@
 // CTA organisation:
 //   warps 0-3  softmax warpgroup for Q tile 0 (rows q0 .. q0+127), one row per thread
 //   warps 4-7  softmax warpgroup for Q tile 1 (rows q0+128 .. q0+255)
-//   warp  8    TMA producer: Q tiles once, then a ring of K and V tiles
+//   warp  8    TMA producer: Q tiles and K_0 once, then a ring whose slot j
+//              holds V_j and K_{j+1}
 //   warp  9    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   S_0 [0,128)  S_1 [128,256)  O_0 [256,256+D)  O_1 [256+D,256+2D)
@@ -62,28 +63,27 @@ template <int D>
 struct Cfg {
     static constexpr int kAtoms = D / 64;                        // 128-byte column blocks per row
     static constexpr uint32_t kTileBytes = (uint32_t)BM * D * 2; // one 128-row bf16 tile
-    // Ring depths.  A V tile is released only after the second Q tile's P V,
-    // one key step later than its K tile, so V gets one stage more.
-    static constexpr int NSTK = D == 128 ? 2 : 4;                // K ring depth
-    static constexpr int NSTV = D == 128 ? 3 : 5;                // V ring depth
+    // Key/value ring: slot j holds V_j and K_{j+1}, the two tiles key step j
+    // of the MMA issuer reads (P_j V_j, then Q K_{j+1}^T), so one full and one
+    // empty barrier per step cover both.  K_0 has a buffer of its own.
+    static constexpr int NSL = D == 128 ? 2 : 4;                 // ring slots
     static constexpr uint32_t kQ = 0;                            // Q_0, Q_1
-    static constexpr uint32_t kK = 2 * kTileBytes;               // K ring
-    static constexpr uint32_t kV = kK + NSTK * kTileBytes;       // V ring
-    static constexpr uint32_t kBar = kV + NSTV * kTileBytes;     // mbarriers
-    static constexpr int kNumBars = 9 + 2 * NSTK + 2 * NSTV;
+    static constexpr uint32_t kK0 = 2 * kTileBytes;              // K_0
+    static constexpr uint32_t kSlot = 3 * kTileBytes;            // slot s: V at +2s tiles, K at +2s+1
+    static constexpr uint32_t kBar = kSlot + 2 * NSL * kTileBytes;  // mbarriers
+    static constexpr int kNumBars = 10 + 2 * NSL;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kSmemBytes = kAbort + 4 + 1024;    // + slack to align the base
     // barrier indices
     __host__ __device__ static constexpr int QF(int t) { return t; }
-    __host__ __device__ static constexpr int KF(int s) { return 2 + s; }
-    __host__ __device__ static constexpr int KE(int s) { return 2 + NSTK + s; }
-    __host__ __device__ static constexpr int VF(int s) { return 2 + 2 * NSTK + s; }
-    __host__ __device__ static constexpr int VE(int s) { return 2 + 2 * NSTK + NSTV + s; }
-    __host__ __device__ static constexpr int SF(int t) { return 2 + 2 * NSTK + 2 * NSTV + t; }
-    __host__ __device__ static constexpr int PF(int t) { return 4 + 2 * NSTK + 2 * NSTV + t; }
-    __host__ __device__ static constexpr int OD(int t) { return 6 + 2 * NSTK + 2 * NSTV + t; }
-    static constexpr int DRAIN = 8 + 2 * NSTK + 2 * NSTV;
+    static constexpr int K0F = 2;
+    __host__ __device__ static constexpr int FULL(int s) { return 3 + s; }
+    __host__ __device__ static constexpr int EMPTY(int s) { return 3 + NSL + s; }
+    __host__ __device__ static constexpr int SF(int t) { return 3 + 2 * NSL + t; }
+    __host__ __device__ static constexpr int PF(int t) { return 5 + 2 * NSL + t; }
+    __host__ __device__ static constexpr int OD(int t) { return 7 + 2 * NSL + t; }
+    static constexpr int DRAIN = 9 + 2 * NSL;
     // tensor-memory columns
     __host__ __device__ static constexpr uint32_t colS(int t) { return (uint32_t)t * 128u; }
     __host__ __device__ static constexpr uint32_t colO(int t) { return 256u + (uint32_t)t * D; }
@@ -186,36 +186,36 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     tma_load_4d_hint(base + C::kQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar(C::QF(t)),
                                      a * 64, q0 + t * BM, hh, bb, pol_q);
             }
-            int issued_k = 0, issued_v = 0;
-            for (int j = 0; j < nk; ++j) {
-                const int s = j % C::NSTK, sv = j % C::NSTV;
-                const uint32_t ph = (uint32_t)(j / C::NSTK) & 1u, phv = (uint32_t)(j / C::NSTV) & 1u;
-                if (!mbar_wait_bounded(bar(C::KE(s)), ph ^ 1u, abort_flag, kWaitLimitNs)) {
-                    record_failure(abort_flag, status);
-                    break;
-                }
-                mbar_expect_tx(bar(C::KF(s)), C::kTileBytes);
+            if (nk > 0) {
+                mbar_expect_tx(bar(C::K0F), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_4d(base + C::kK + s * C::kTileBytes + a * kAtomBytes, &tmK, bar(C::KF(s)),
-                                a * 64, (jb + j) * BN, hh, bb);
-                issued_k = j + 1;
-                if (!mbar_wait_bounded(bar(C::VE(sv)), phv ^ 1u, abort_flag, kWaitLimitNs)) {
-                    record_failure(abort_flag, status);
-                    break;
-                }
-                mbar_expect_tx(bar(C::VF(sv)), C::kTileBytes);
-                for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_4d(base + C::kV + sv * C::kTileBytes + a * kAtomBytes, &tmV, bar(C::VF(sv)),
-                                a * 64, (jb + j) * BN, hh, bb);
-                issued_v = j + 1;
+                    tma_load_4d(base + C::kK0 + a * kAtomBytes, &tmK, bar(C::K0F), a * 64, jb * BN, hh, bb);
             }
-            // Drain: the last copy issued into each stage has landed before the
+            int issued = 0;
+            for (int c = 0; c < nk; ++c) {
+                const int sl = c % C::NSL;
+                const uint32_t ph = (uint32_t)(c / C::NSL) & 1u;
+                if (!mbar_wait_bounded(bar(C::EMPTY(sl)), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                    record_failure(abort_flag, status);
+                    break;
+                }
+                const bool kn = c + 1 < nk;
+                const uint32_t vdst = base + C::kSlot + 2u * sl * C::kTileBytes;
+                mbar_expect_tx(bar(C::FULL(sl)), kn ? 2 * C::kTileBytes : C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_4d(vdst + a * kAtomBytes, &tmV, bar(C::FULL(sl)), a * 64, (jb + c) * BN, hh, bb);
+                if (kn)
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_load_4d(vdst + C::kTileBytes + a * kAtomBytes, &tmK, bar(C::FULL(sl)), a * 64,
+                                    (jb + c + 1) * BN, hh, bb);
+                issued = c + 1;
+            }
+            // Drain: the last copy issued into each slot has landed before the
             // CTA may exit (returns at once on the normal path, where every
             // copy has been consumed).
-            for (int j = max(0, issued_k - C::NSTK); j < issued_k; ++j)
-                mbar_wait_bounded(bar(C::KF(j % C::NSTK)), (uint32_t)(j / C::NSTK) & 1u, nullptr, kWaitLimitNs);
-            for (int j = max(0, issued_v - C::NSTV); j < issued_v; ++j)
-                mbar_wait_bounded(bar(C::VF(j % C::NSTV)), (uint32_t)(j / C::NSTV) & 1u, nullptr, kWaitLimitNs);
+            for (int c = max(0, issued - C::NSL); c < issued; ++c)
+                mbar_wait_bounded(bar(C::FULL(c % C::NSL)), (uint32_t)(c / C::NSL) & 1u, nullptr, kWaitLimitNs);
+            if (nk > 0) mbar_wait_bounded(bar(C::K0F), 0, nullptr, kWaitLimitNs);
             for (int t = 0; t < 2; ++t)
                 if ((t == 0 ? n0 : n1) > 0) mbar_wait_bounded(bar(C::QF(t)), 0, nullptr, kWaitLimitNs);
         }
@@ -232,63 +232,103 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // 14 bits) of every operand block follows by adding its offset / 16
             // (shared addresses stay below 256 KB, so the field cannot carry).
             const uint64_t dQ = umma_desc_sw128(base + C::kQ, 16, 1024);
-            const uint64_t dK = umma_desc_sw128(base + C::kK, 16, 1024);
-            const uint64_t dV = umma_desc_sw128(base + C::kV, kAtomBytes, 1024);
-            auto issue_S = [&](int t, int s) {
+            const uint64_t dK0 = umma_desc_sw128(base + C::kK0, 16, 1024);
+            const uint64_t dK = umma_desc_sw128(base + C::kSlot + C::kTileBytes, 16, 1024);
+            const uint64_t dV = umma_desc_sw128(base + C::kSlot, kAtomBytes, 1024);
+            constexpr uint32_t kSlotStep = 2 * C::kTileBytes >> 4;
+            // kb: descriptor of the K tile (K_0's buffer or a slot's K half)
+            auto issue_S = [&](int t, uint64_t kb) {
                 const uint64_t qa = dQ + ((uint32_t)t * C::kTileBytes >> 4);
-                const uint64_t kb = dK + ((uint32_t)s * C::kTileBytes >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((uint32_t)(kk >> 2) * kAtomBytes + (uint32_t)(kk & 3) * 32u) >> 4;
                     mma_ss(tmem + C::colS(t), qa + off, kb + off, idS, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_PV = [&](int t, int s, bool acc) {
-                const uint64_t vb = dV + ((uint32_t)s * C::kTileBytes >> 4);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    mma_ts(tmem + C::colO(t), tmem + C::colS(t) + (uint32_t)kk * 8u, vb + ((uint32_t)kk * 2048u >> 4), idO,
-                           (acc || kk > 0) ? 1u : 0u);
-                }
-            };
             bool ok = true;
             for (int t = 0; t < 2 && ok; ++t)
                 if (nt[t] > 0) ok = mbar_wait_bounded(bar(C::QF(t)), 0, abort_flag, kWaitLimitNs);
             // (a split may hold no key tile at all: then nothing is issued)
-            if (ok && nk > 0) ok = mbar_wait_bounded(bar(C::KF(0)), 0, abort_flag, kWaitLimitNs);
+            if (ok && nk > 0) ok = mbar_wait_bounded(bar(C::K0F), 0, abort_flag, kWaitLimitNs);
             if (ok && nk > 0) {
                 tc_fence_after();
                 for (int t = 0; t < 2; ++t) {
                     if (nt[t] == 0) continue;
-                    issue_S(t, 0);
+                    issue_S(t, dK0);
                     mma_commit(bar(C::SF(t)));
                 }
-                mma_commit(bar(C::KE(0)));
             }
+            // MMAs go out in groups of four, each also sampling an mbarrier whose
+            // answer is read only after the group: tile 0's last group samples
+            // P_1 of this step, tile 1's first group the next step's K/V slot
+            // and its last group P_0 of the next step.  A barrier found
+            // complete is not waited for again; the sample's round trip hides
+            // behind the MMA issue (each wait would otherwise idle the pipe).
+            auto pv_quad = [&](int t, int sl, int q, uint32_t acc, uint32_t sbar, uint32_t spar) -> bool {
+                const uint64_t vb = dV + (uint32_t)sl * kSlotStep + (uint32_t)q * 512u;
+                return mma4_ts_sample(tmem + C::colO(t), tmem + C::colS(t) + (uint32_t)q * 32u, vb, vb + 128u,
+                                      vb + 256u, vb + 384u, idO, acc, sbar, spar);
+            };
+            auto s_quad = [&](int t, uint64_t kb, int q, uint32_t sbar, uint32_t spar) -> bool {
+                const uint64_t qa = dQ + ((uint32_t)t * C::kTileBytes >> 4) + (uint32_t)q * (kAtomBytes >> 4);
+                const uint64_t kq = kb + (uint32_t)q * (kAtomBytes >> 4);
+                return mma4_ss_sample(tmem + C::colS(t), qa, qa + 2u, qa + 4u, qa + 6u, kq, kq + 2u, kq + 4u, kq + 6u,
+                                      idS, q > 0 ? 1u : 0u, sbar, spar);
+            };
+            constexpr int kSQuads = D / 64;
+            bool full_ok = false, pf0_ok = false;
             for (int j = 0; j < nk && ok; ++j) {
-                const int s = j % C::NSTV;
-                const uint32_t ph = (uint32_t)(j / C::NSTV) & 1u;
+                const int sl = j % C::NSL;
+                const uint32_t ph = (uint32_t)(j / C::NSL) & 1u;
+                const uint32_t pj = (uint32_t)j & 1u;
                 const int jn = j + 1;
-                const int sn = jn % C::NSTK;
-                const uint32_t phn = (uint32_t)(jn / C::NSTK) & 1u;
-                // Both operand tiles of this step are waited for up front, so a
-                // tile's P V and its next Q K^T go to the tensor pipe back to back.
-                const bool kn_ready = jn < nk;
-                if (!(ok = mbar_wait_bounded(bar(C::VF(s)), ph, abort_flag, kWaitLimitNs))) break;
-                if (kn_ready && !(ok = mbar_wait_bounded(bar(C::KF(sn)), phn, abort_flag, kWaitLimitNs))) break;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= nt[t]) continue;
-                    if (!(ok = mbar_wait_bounded(bar(C::PF(t)), (uint32_t)j & 1u, abort_flag, kWaitLimitNs))) break;
+                // V_j and K_{j+1}, then per Q tile P_j V_j and Q K_{j+1}^T back to back
+                if (!full_ok && !(ok = mbar_wait_bounded(bar(C::FULL(sl)), ph, abort_flag, kWaitLimitNs))) break;
+                full_ok = false;
+                bool pf1_ok = false, pf0_next = false;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (!ok || j >= nt[t]) continue;
+                    const bool ready = t == 0 ? pf0_ok : pf1_ok;
+                    if (!ready && !(ok = mbar_wait_bounded(bar(C::PF(t)), pj, abort_flag, kWaitLimitNs))) break;
                     tc_fence_after();
-                    issue_PV(t, s, j > 0);
-                    if (j == nt[t] - 1) mma_commit(bar(C::OD(t)));
-                    if (jn < nt[t]) {
-                        issue_S(t, sn);
+                    // sample targets; QF(t) (long complete) where there is nothing to sample
+                    const uint32_t dummy = bar(C::QF(t));
+                    uint32_t fb = dummy, fp = 0, lb = dummy, lp = 0;
+                    if (t == 1 && jn < nk) {
+                        fb = bar(C::FULL(jn % C::NSL));
+                        fp = (uint32_t)(jn / C::NSL) & 1u;
+                    }
+                    if (t == 0 && j < nt[1]) {
+                        lb = bar(C::PF(1));
+                        lp = pj;
+                    }
+                    if (t == 1 && jn < nt[0]) {
+                        lb = bar(C::PF(0));
+                        lp = pj ^ 1u;
+                    }
+                    const bool has_next = jn < nt[t];
+                    const bool f_res = pv_quad(t, sl, 0, j > 0 ? 1u : 0u, fb, fp);
+                    bool l_res;
+                    if (!has_next) {
+                        l_res = pv_quad(t, sl, 1, 1u, lb, lp);
+                        if (j == nt[t] - 1) mma_commit(bar(C::OD(t)));
+                    } else {
+                        pv_quad(t, sl, 1, 1u, dummy, 0);
+                        const uint64_t kb = dK + (uint32_t)sl * kSlotStep;
+#pragma unroll
+                        for (int q = 0; q + 1 < kSQuads; ++q) s_quad(t, kb, q, dummy, 0);
+                        l_res = s_quad(t, kb, kSQuads - 1, lb, lp);
                         mma_commit(bar(C::SF(t)));
                     }
+                    if (t == 0) pf1_ok = l_res && lb != dummy;
+                    if (t == 1) {
+                        full_ok = f_res && fb != dummy;
+                        pf0_next = l_res && lb != dummy;
+                    }
                 }
-                mma_commit(bar(C::VE(s)));
-                if (kn_ready) mma_commit(bar(C::KE(sn)));
+                mma_commit(bar(C::EMPTY(sl)));
+                pf0_ok = pf0_next;
             }
             if (!ok) record_failure(abort_flag, status);
             // Drain: every MMA issued above has completed before TMEM is freed.
