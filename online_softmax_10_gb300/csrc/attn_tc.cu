@@ -105,6 +105,57 @@ __device__ __forceinline__ int kv_tiles_for(int q0, int t, int N, int M, int cof
     return (int)min((long)nM, last_key / BN + 1);
 }
 
+// Four MMAs into one accumulator (the first accumulates if `acc`), preceded by
+// a non-blocking sample of an mbarrier phase whose result is read only after
+// the fourth MMA: the barrier's round trip to shared memory then overlaps the
+// MMA issue instead of stalling the thread (a predicate cannot outlive one asm
+// block, so both live in the same one).  Returns true if the phase with the
+// given parity had completed when sampled.
+__device__ __forceinline__ bool mma4_ss_sample(uint32_t d_tmem, uint64_t a0, uint64_t a1, uint64_t a2, uint64_t a3,
+                                               uint64_t b0, uint64_t b1, uint64_t b2, uint64_t b3, uint32_t idesc,
+                                               uint32_t acc, uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred pt, pa, p1;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 pt, [%12], %13;\n\t"
+        "setp.ne.b32 pa, %11, 0;\n\t"
+        "setp.eq.u32 p1, 0, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %6, %10, pa;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], %3, %7, %10, p1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], %4, %8, %10, p1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], %5, %9, %10, p1;\n\t"
+        "selp.u32 %0, 1, 0, pt;\n\t}"
+        : "=r"(done)
+        : "r"(d_tmem), "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
+          "r"(acc), "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// The same with A read from tensor memory at a, a + 8, a + 16, a + 24 columns.
+__device__ __forceinline__ bool mma4_ts_sample(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint64_t b1, uint64_t b2,
+                                               uint64_t b3, uint32_t idesc, uint32_t acc, uint32_t bar,
+                                               uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred pt, pa, p1;\n\t.reg .b32 a1, a2, a3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 pt, [%9], %10;\n\t"
+        "setp.ne.b32 pa, %8, 0;\n\t"
+        "setp.eq.u32 p1, 0, 0;\n\t"
+        "add.u32 a1, %2, 8;\n\t"
+        "add.u32 a2, %2, 16;\n\t"
+        "add.u32 a3, %2, 24;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %7, pa;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], %4, %7, p1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], %5, %7, p1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], %6, %7, p1;\n\t"
+        "selp.u32 %0, 1, 0, pt;\n\t}"
+        : "=r"(done)
+        : "r"(d_tmem), "r"(a_tmem), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc), "r"(acc), "r"(bar),
+          "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 __device__ __forceinline__ void record_failure(volatile int* abort_flag, int* status) {
     *abort_flag = 1;
     atomicExch(status, kDevStatusTimeout);
