@@ -111,6 +111,21 @@ def workload_rows_inputs(w: RowsWorkload):
     return rows_inputs(w.rows, w.cols, w.dtype, w.seed, w.sigma, w.spike)
 
 
+def device_normal(shape, seed: int, sigma: float = 1.0, dtype=torch.bfloat16, device="cuda"):
+    """Seeded N(0, sigma^2) values drawn on the device and cast to ``dtype``
+    (round to nearest), for inputs too large to draw on the host.  Drawn in
+    slices of 2^28 values so the fp32 temporary stays at 1 GiB."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    out = torch.empty(shape, dtype=dtype, device=device)
+    flat = out.view(-1)
+    step = 1 << 28
+    for s in range(0, flat.numel(), step):
+        e = min(flat.numel(), s + step)
+        flat[s:e] = (torch.randn(e - s, generator=g, device=device) * sigma).to(dtype)
+    return out
+
+
 def sample_rows(total: int, count: int, seed: int = 12345):
     """A seeded, sorted sample of ``count`` distinct indices in [0, total),
     always including the first and the last index (edge rows)."""

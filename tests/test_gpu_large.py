@@ -1,0 +1,96 @@
+"""Maximum sizes: tensors past 2^31 elements (the kernels' element offsets
+must be 64-bit) and a million-key split-KV problem, each checked on sampled
+rows against the fp64 oracle.  Tolerances as in the other parity tests.
+
+Inputs are drawn on the device (seeded, inputs.device_normal); the sampled
+rows and the heads they need are copied back and given to the oracle, so both
+sides see the same bits.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from online_softmax_10_gb300 import fattn, inputs
+from parity import BF16_HALF_ULP_REL, O_TOL_BF16, P_TOL_BF16, ensure_built, lse_ok, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    yield
+    torch.cuda.empty_cache()
+
+
+def _edge_and_sample(total, count, seed):
+    rows = {0, total - 1}
+    rows.update(int(r) for r in inputs.sample_rows(total, count, seed=seed))
+    return np.array(sorted(rows))
+
+
+# (rows, cols): the pipelined kernel (64 KB rows), the one-CTA-per-row kernel
+# (8 KB rows) and the streaming kernel (> 64K columns), each past 2^31 elements
+ROW_SHAPES = [(65600, 32768), (525000, 4096), (21500, 100000)]
+
+
+@pytest.mark.parametrize("rows,cols", ROW_SHAPES)
+def test_softmax_rows_past_2p31_elements(rows, cols):
+    assert rows * cols > 2 ** 31
+    x = inputs.device_normal((rows, cols), seed=rows + cols, sigma=3.0)
+    p, lse = fattn.softmax_rows(x)
+    lse2 = fattn.logsumexp_rows(x)
+    assert fattn.device_status() == fattn.FA_OK
+    sel = _edge_and_sample(rows, 30, seed=cols)
+    idx = torch.as_tensor(sel, device=x.device)
+    P_ref, L_ref = oracle.softmax_rows(x[idx].cpu())
+    err = float(np.max(np.abs(to_np(p[idx]) - P_ref)))
+    assert err <= P_TOL_BF16, err
+    for got in (lse, lse2):
+        ok, rel = lse_ok(to_np(got[idx]), L_ref)
+        assert ok, rel
+    sums = p.sum(dim=1, dtype=torch.float32)
+    assert torch.all((sums - 1).abs() <= 1e-2).item()
+
+
+def test_attention_past_2p31_elements():
+    # B=17 H=64 N=M=16384 d=128: 2.28e9 elements per tensor, causal
+    B, H, N, d = 17, 64, 16384, 128
+    q = inputs.device_normal((B, H, N, d), seed=71)
+    k = inputs.device_normal((B, H, N, d), seed=72)
+    v = inputs.device_normal((B, H, N, d), seed=73)
+    assert q.numel() > 2 ** 31
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fattn.attn_fwd(q, k, v, scale, True)
+    assert fattn.device_status() == fattn.FA_OK
+    for (b, h) in [(0, 0), (8, 31), (B - 1, H - 1)]:
+        sel = _edge_and_sample(N, 14, seed=b * H + h)
+        qh, kh, vh = (t[b:b + 1, h:h + 1].cpu() for t in (q, k, v))
+        O_ref, L_ref = oracle.attn_fwd(qh, kh, vh, scale, True, rows=sel)
+        O_g = to_np(o[b, h])[sel]
+        tol = O_TOL_BF16 + BF16_HALF_ULP_REL * np.abs(O_ref)
+        assert np.all(np.abs(O_g - O_ref) <= tol), float(np.max(np.abs(O_g - O_ref)))
+        ok, rel = lse_ok(to_np(lse[b, h])[sel], L_ref)
+        assert ok, rel
+    del q, k, v, o, lse
+
+
+def test_splitkv_million_keys():
+    # decode-like: 64 queries per head against 2^20 keys, split over CTAs
+    B, H, N, M, d = 1, 2, 64, 1 << 20, 128
+    q = inputs.device_normal((B, H, N, d), seed=81)
+    k = inputs.device_normal((B, H, M, d), seed=82)
+    v = inputs.device_normal((B, H, M, d), seed=83)
+    scale = 1.0 / math.sqrt(d)
+    assert fattn.splitkv_num_splits(B, H, N, M, d, False) > 1
+    o, lse = fattn.attn_fwd_splitkv(q, k, v, scale, False, out_dtype=torch.float32)
+    assert fattn.device_status() == fattn.FA_OK
+    sel = _edge_and_sample(B * H * N, 14, seed=5)
+    O_ref, L_ref = oracle.attn_fwd(q.cpu(), k.cpu(), v.cpu(), scale, False, rows=sel)
+    O_g = to_np(o).reshape(-1, d)[sel]
+    assert float(np.max(np.abs(O_g - O_ref))) <= O_TOL_BF16
+    ok, rel = lse_ok(to_np(lse).reshape(-1)[sel], L_ref)
+    assert ok, rel
