@@ -37,6 +37,7 @@ namespace fa {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2f = 0.6931471805599453f;
 
 template <typename T>
 struct Elem;
@@ -628,12 +629,16 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
                 m = mn;
             }
         }
+        // warp merge in two passes: the max first (no exponentials in the
+        // shuffle chain), then every lane's sum rescaled to it once and added
+        float wm = m;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
-            const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-            merge_ms(m, sum, m2, s2);
-        }
+        for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+        float ws = wm == -CUDART_INF_F ? 0.f : sum * ex2((m - wm) * kLog2e);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, off);
+        m = wm;
+        sum = ws;
         float2* slot = red + (g * 2 + (k & 1)) * WG;
         if (lane == 0) slot[gw] = make_float2(m, sum);
         __syncwarp();
@@ -646,15 +651,15 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
             break;
         }
         if (gw == 0) {
+            // the same two passes over the group's WG warp results
             const float2 a = slot[lane & (WG - 1)];
-            float M = a.x, S = a.y;
+            float M = a.x;
 #pragma unroll
-            for (int off = WG / 2; off > 0; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, M, off);
-                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, S, off);
-                merge_ms(M, S, m2, s2);
-            }
-            if (lane == 0) write_row_lse(X, r, cols, M + logf(S), LSE, labels, loss);
+            for (int off = WG / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+            float S = M == -CUDART_INF_F ? 0.f : a.y * ex2((a.x - M) * kLog2e);
+#pragma unroll
+            for (int off = WG / 2; off > 0; off >>= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, off);
+            if (lane == 0) write_row_lse(X, r, cols, M + __log2f(S) * kLn2f, LSE, labels, loss);
         }
     }
 }
