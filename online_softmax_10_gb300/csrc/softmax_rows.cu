@@ -705,7 +705,9 @@ bool try_launch_lse_tma(const TIn* X, float* LSE, long rows, long cols, int* sta
                         cudaError_t* err, const long long* labels, float* loss) {
     constexpr int V = Elem<TIn>::kVec;
     const long row_bytes = cols * (long)sizeof(TIn);
-    if (cols % V != 0 || row_bytes < 16384 || row_bytes > 65536 || rows < 64) return false;
+    // (rows of 16 KB and less: one 128-thread CTA per row streams them faster,
+    // 16384 x 8192 bf16 in 71.8 us against 84.2 here)
+    if (cols % V != 0 || row_bytes <= 16384 || row_bytes > 65536 || rows < 64) return false;
     const long nvec = cols / V;
     const uint32_t stage = (uint32_t)((row_bytes + 127) / 128 * 128);
     int nst = (int)(kTmaSmemBudget / stage);
