@@ -188,6 +188,32 @@ def time_launches(fn, steps: int, warmup: int, world_size: int):
     return max_over_ranks(total, world_size, device="cuda"), per
 
 
+def time_graph(fn, calls: int, reps: int):
+    """Mean device seconds per fn() call: `calls` calls captured in one CUDA
+    graph, replayed `reps` times between CUDA events (launches back to back,
+    no host work between them)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(reps):
+        g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3 / (calls * reps)
+
+
 # ------------------------------------------------------------------ CPU oracle
 def cpu_oracle_sample(w, target_s: float = 10.0, max_rows: int | None = None):
     """Time the fp64 oracle on a seeded sample of the workload's query rows.
@@ -372,6 +398,11 @@ def run_ours(args, world_size, rank, local_rank):
     fq, fk, fv = (t.cuda() for t in inputs.workload_attn_inputs(fw))
     f_total, f_per = time_launches(lambda: fattn.attn_fwd(fq, fk, fv, fw.scale, fw.causal), 200, 10, world_size)
     assert fattn.device_status() == fattn.FA_OK
+    # the kernel's own time: the same call (outputs preallocated) captured 50
+    # times in a CUDA graph and replayed, so no host work paces the launches
+    fo, fl = torch.empty_like(fq), torch.empty(fq.shape[:3], dtype=torch.float32, device=fq.device)
+    f_dev = time_graph(lambda: fattn.attn_fwd(fq, fk, fv, fw.scale, fw.causal, out=fo, lse=fl), 50, 5)
+    assert fattn.device_status() == fattn.FA_OK
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -413,7 +444,8 @@ def run_ours(args, world_size, rank, local_rank):
                          "value": s_flops / s_per / 1e12, "unit": "TFLOP/s", "us_per_launch": s_per * 1e6,
                          "unsplit_value": s_flops / u_per / 1e12},
         "attn_f32": {"workload": fw.name, "us_per_launch": f_per * 1e6,
-                     "value": fw.flops() / f_per / 1e12, "unit": "TFLOP/s"},
+                     "value": fw.flops() / f_per / 1e12, "unit": "TFLOP/s",
+                     "device_us_per_launch": f_dev * 1e6},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

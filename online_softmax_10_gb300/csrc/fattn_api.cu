@@ -160,7 +160,7 @@ int attn_launch(const void* Q, const void* K, const void* V, void* O, float* LSE
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (in_dtype == FA_F32) {
-        e = fa::launch_attn_f32(p, cs);
+        e = fa::launch_attn_f32(p, num_sms(), cs);
     } else {
         CUtensorMap tq, tk, tv;
         if (!encode_bf16_4d(&tq, Q, B, H, N, d, st.q) || !encode_bf16_4d(&tk, K, B, H, M, d, st.k) ||

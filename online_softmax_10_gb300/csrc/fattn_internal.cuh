@@ -41,7 +41,7 @@ cudaError_t launch_logsumexp_rows(const void* X, float* LSE, long rows, long col
                                   const long long* labels, float* loss, int* status, cudaStream_t stream);
 
 // fp32 CUDA-core attention (attn_f32.cu).  d in {16, 32, 64, 128}.
-cudaError_t launch_attn_f32(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_attn_f32(const AttnParams& p, int num_sms, cudaStream_t stream);
 
 // bf16 tensor-core attention (attn_tc.cu).  d in {64, 128}.  The three tensor
 // maps describe Q [B, H, N, d], K and V [B, H, M, d] (any strides) as 4-D bf16

@@ -44,6 +44,17 @@ def test_f32_shapes(d, causal, N, M):
     assert ok, rel
 
 
+@pytest.mark.parametrize("d", [16, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_f32_many_row_blocks(d, causal):
+    """Enough 64-row blocks (32 heads x 10) to fill the GPU twice over: the
+    kernel takes 64 rows per CTA instead of 16; ragged last block."""
+    q, k, v = inputs.attn_inputs(4, 8, 610, 610, d, torch.float32, seed=610 + d)
+    err, ratio, ok, rel = attn_case(q, k, v, causal)
+    assert ratio <= 1.0, err
+    assert ok, rel
+
+
 # ----------------------------------------------------------------- bf16 tensor-core path
 BF16_SHAPES = [(1, 1), (1, 300), (127, 127), (128, 128), (129, 129), (255, 255), (256, 256), (257, 257),
                (300, 100), (100, 300), (513, 2100), (1000, 1000)]
