@@ -108,6 +108,18 @@ __device__ __forceinline__ void store_out<__nv_bfloat16, 8>(__nv_bfloat16* p, co
     }
 }
 
+// Element-wise max of two bf16 pairs (exact: bf16 values order as their floats).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// -inf in every element of a 32-bit word: two bf16, or one fp32
+template <typename T>
+__host__ __device__ constexpr uint32_t neg_inf_word() {
+    return sizeof(T) == 2 ? 0xFF80FF80u : 0xFF800000u;
+}
+
 // (m, s) <- (m, s) (+) (m2, s2): the pairwise online-normaliser update.
 // Sums are relative to their own max; an empty partial is (-inf, 0).
 __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
@@ -497,8 +509,6 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
                    int nst, int* status, const long long* __restrict__ labels, float* __restrict__ loss) {
     constexpr int V = Elem<TIn>::kVec;
     constexpr int WG = kLseGroupThreads / 32;  // warps per group
-    constexpr int CH = 4;                      // vectors per online step
-    static_assert(NV % (2 * CH) == 0, "NV must be a multiple of two chunks");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 127u) & ~127u;
@@ -567,67 +577,70 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
             atomicExch(status, kDevStatusTimeout);
             break;
         }
-        // this thread's slice in two halves, still packed; the stage goes back
-        // to the producer as soon as the second half is in registers
+        // this thread's slice, still packed, into registers; the stage goes
+        // back to the producer as soon as it is loaded
         const TIn* srow = reinterpret_cast<const TIn*>(gbase + (uint32_t)s * stage_bytes);
-        constexpr int NH = NV / 2;
-        const bool whole_slice = (long)NV * kLseGroupThreads <= nvec;
-        float m = -CUDART_INF_F, sum = 0.f;
+        uint4 raw[NV];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint4 raw[NH];
+        for (int kk = 0; kk < NV; ++kk) {
+            const long vi = gt + (long)kk * kLseGroupThreads;
+            // (past the row end: -inf, which neither the max nor the sum sees)
+            constexpr uint32_t ni = neg_inf_word<TIn>();
+            raw[kk] = vi < nvec ? *reinterpret_cast<const uint4*>(srow + vi * V) : make_uint4(ni, ni, ni, ni);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));
+        // the slice max first (bf16: on the packed pairs), then one exponential
+        // per element relative to it
+        float m;
+        if constexpr (V == 8) {
+            uint32_t mw[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
 #pragma unroll
-            for (int kk = 0; kk < NH; ++kk) {
-                const long vi = gt + (long)(half * NH + kk) * kLseGroupThreads;
-                raw[kk] = vi < nvec ? *reinterpret_cast<const uint4*>(srow + vi * V) : make_uint4(0, 0, 0, 0);
+            for (int kk = 1; kk < NV; ++kk) {
+                mw[0] = bf16x2_max(mw[0], raw[kk].x);
+                mw[1] = bf16x2_max(mw[1], raw[kk].y);
+                mw[2] = bf16x2_max(mw[2], raw[kk].z);
+                mw[3] = bf16x2_max(mw[3], raw[kk].w);
             }
-            if (half == 1) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty(s));
+            const uint32_t w = bf16x2_max(bf16x2_max(mw[0], mw[1]), bf16x2_max(mw[2], mw[3]));
+            m = fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+        } else {
+            float mf[4] = {__uint_as_float(raw[0].x), __uint_as_float(raw[0].y), __uint_as_float(raw[0].z),
+                           __uint_as_float(raw[0].w)};
+#pragma unroll
+            for (int kk = 1; kk < NV; ++kk) {
+                mf[0] = fmaxf(mf[0], __uint_as_float(raw[kk].x));
+                mf[1] = fmaxf(mf[1], __uint_as_float(raw[kk].y));
+                mf[2] = fmaxf(mf[2], __uint_as_float(raw[kk].z));
+                mf[3] = fmaxf(mf[3], __uint_as_float(raw[kk].w));
             }
+            m = fmaxf(fmaxf(mf[0], mf[1]), fmaxf(mf[2], mf[3]));
+        }
+        float sum = 0.f;
+        if (m != -CUDART_INF_F) {
+            // only the sum is kept, so the exponent is one packed FMA:
+            // x log2e - m log2e (enough precision for log-sum-exp)
+            const float2 nmc = make_float2(-m * kLog2e, -m * kLog2e);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int k0 = 0; k0 < NH; k0 += CH) {
-                float v[CH][V];
+            for (int kk = 0; kk < NV; ++kk) {
+                const uint32_t w[4] = {raw[kk].x, raw[kk].y, raw[kk].z, raw[kk].w};
 #pragma unroll
-                for (int kk = 0; kk < CH; ++kk) {
-                    // (whole_slice: every vector of this thread is in the row; no per-element select)
-                    const bool in = whole_slice || gt + (long)(half * NH + k0 + kk) * kLseGroupThreads < nvec;
-                    const uint4 u = raw[k0 + kk];
+                for (int e = 0; e < 4; ++e) {
+                    float2 x2;
                     if constexpr (V == 8) {
-                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            v[kk][2 * e] = in ? __uint_as_float(w[e] << 16) : -CUDART_INF_F;
-                            v[kk][2 * e + 1] = in ? __uint_as_float(w[e] & 0xFFFF0000u) : -CUDART_INF_F;
-                        }
+                        x2 = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
                     } else {
-                        v[kk][0] = in ? __uint_as_float(u.x) : -CUDART_INF_F;
-                        v[kk][1] = in ? __uint_as_float(u.y) : -CUDART_INF_F;
-                        v[kk][2] = in ? __uint_as_float(u.z) : -CUDART_INF_F;
-                        v[kk][3] = in ? __uint_as_float(u.w) : -CUDART_INF_F;
+                        if (e & 1) continue;
+                        x2 = make_float2(__uint_as_float(w[e]), __uint_as_float(w[e + 1]));
                     }
+                    const float2 t2 = fma2(x2, cc, nmc);
+                    acc[e] = add2(acc[e], make_float2(ex2(t2.x), ex2(t2.y)));
                 }
-                float cm = -CUDART_INF_F;
-#pragma unroll
-                for (int kk = 0; kk < CH; ++kk)
-#pragma unroll
-                    for (int e = 0; e < V; e += 2) cm = max3f(cm, v[kk][e], v[kk][e + 1]);
-                if (cm == -CUDART_INF_F) continue;
-                const float mn = fmaxf(m, cm);
-                // only the sum is kept, so the exponent is one packed FMA:
-                // x log2e - mn log2e (enough precision for log-sum-exp)
-                const float2 nmc = make_float2(-mn * kLog2e, -mn * kLog2e);
-                float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int kk = 0; kk < CH; ++kk)
-#pragma unroll
-                    for (int e = 0; e < V; e += 2) {
-                        const float2 t2 = fma2(make_float2(v[kk][e], v[kk][e + 1]), cc, nmc);
-                        acc = add2(acc, make_float2(ex2(t2.x), ex2(t2.y)));
-                    }
-                sum = sum * ex2((m - mn) * kLog2e) + (acc.x + acc.y);
-                m = mn;
             }
+            const float2 a2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+            sum = a2.x + a2.y;
         }
         // warp merge in two passes: the max first (no exponentials in the
         // shuffle chain), then every lane's sum rescaled to it once and added
