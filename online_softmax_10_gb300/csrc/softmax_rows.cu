@@ -120,6 +120,53 @@ __host__ __device__ constexpr uint32_t neg_inf_word() {
     return sizeof(T) == 2 ? 0xFF80FF80u : 0xFF800000u;
 }
 
+// Packed fp32x2 a - b and a * b (round to nearest).
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+// Max over a thread's packed slice: on bf16 pairs (exact), or on fp32 words.
+template <typename TIn, int NV>
+__device__ __forceinline__ float slice_max(const uint4* raw) {
+    if constexpr (sizeof(TIn) == 2) {
+        uint32_t mw[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
+#pragma unroll
+        for (int k = 1; k < NV; ++k) {
+            mw[0] = bf16x2_max(mw[0], raw[k].x);
+            mw[1] = bf16x2_max(mw[1], raw[k].y);
+            mw[2] = bf16x2_max(mw[2], raw[k].z);
+            mw[3] = bf16x2_max(mw[3], raw[k].w);
+        }
+        const uint32_t w = bf16x2_max(bf16x2_max(mw[0], mw[1]), bf16x2_max(mw[2], mw[3]));
+        return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    } else {
+        float mf[4] = {__uint_as_float(raw[0].x), __uint_as_float(raw[0].y), __uint_as_float(raw[0].z),
+                       __uint_as_float(raw[0].w)};
+#pragma unroll
+        for (int k = 1; k < NV; ++k) {
+            mf[0] = fmaxf(mf[0], __uint_as_float(raw[k].x));
+            mf[1] = fmaxf(mf[1], __uint_as_float(raw[k].y));
+            mf[2] = fmaxf(mf[2], __uint_as_float(raw[k].z));
+            mf[3] = fmaxf(mf[3], __uint_as_float(raw[k].w));
+        }
+        return fmaxf(fmaxf(mf[0], mf[1]), fmaxf(mf[2], mf[3]));
+    }
+}
+
 // (m, s) <- (m, s) (+) (m2, s2): the pairwise online-normaliser update.
 // Sums are relative to their own max; an empty partial is (-inf, 0).
 __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
@@ -320,7 +367,10 @@ constexpr uint32_t kTmaSmemExtra = 128 /* alignment */ + kTmaBarBytes + 2 * 16 *
 
 // One CTA per SM; rows r = blockIdx.x + i * gridDim.x go through a ring of
 // `nst` shared-memory stages of `stage_bytes` each.
-template <typename TIn, typename TOut, bool WRITE_P, int NV, bool LOGP>
+// PACKED: the slice stays packed until the exponent pass, which runs on
+// fp32 pairs (faster with four or more stages in the ring; with three, at
+// 64 KB rows, the unpacked form is).
+template <typename TIn, typename TOut, bool WRITE_P, int NV, bool LOGP, bool PACKED>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restrict__ LSE, long rows, long cols,
                  uint32_t stage_bytes, int nst, int* status) {
@@ -394,47 +444,86 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
             atomicExch(status, kDevStatusTimeout);
             break;
         }
-        // the row slice into registers, then the stage goes back to the producer
+        // the row slice into registers, then the stage goes back to the
+        // producer; v becomes exp(x - m) for this thread's max m (log p keeps
+        // x itself).  A slice that is all -inf (masked logits) takes m = 0 for
+        // the exponent, so every p = exp(-inf) = 0 and the sum is 0.
         const TIn* srow = reinterpret_cast<const TIn*>(gbase + (uint32_t)s * stage_bytes);
         float v[NV][V];
+        float m, sum;
+        if constexpr (PACKED) {
+            // loaded packed; the max on the packed words (bf16 pairs: exact),
+            // the exponent arguments two lanes at a time
+            uint4 raw[NV];
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const long vi = threadIdx.x + (long)k * kTmaConsumers;
-            if (vi < nvec) {
-                const uint4 u = *reinterpret_cast<const uint4*>(srow + vi * V);
-                if constexpr (V == 8) {
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            for (int k = 0; k < NV; ++k) {
+                const long vi = threadIdx.x + (long)k * kTmaConsumers;
+                constexpr uint32_t ni = neg_inf_word<TIn>();
+                raw[k] = vi < nvec ? *reinterpret_cast<const uint4*>(srow + vi * V) : make_uint4(ni, ni, ni, ni);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(s));
+            m = slice_max<TIn, NV>(raw);
+            const float mk = m == -CUDART_INF_F ? 0.f : m;
+            const float2 mm = make_float2(mk, mk), kk2 = make_float2(kc, kc);
+            float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        v[k][2 * e] = __uint_as_float(w[e] << 16);
-                        v[k][2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            for (int k = 0; k < NV; ++k) {
+                const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+                for (int e = 0; e < V; e += 2) {
+                    float2 x2;
+                    if constexpr (V == 8) {
+                        x2 = make_float2(__uint_as_float(w[e / 2] << 16), __uint_as_float(w[e / 2] & 0xFFFF0000u));
+                    } else {
+                        x2 = make_float2(__uint_as_float(w[e]), __uint_as_float(w[e + 1]));
+                    }
+                    const float2 t2 = mul2(sub2(x2, mm), kk2);
+                    const float2 ex = make_float2(ex2(t2.x), ex2(t2.y));
+                    v[k][e] = LOGP ? x2.x : ex.x;
+                    v[k][e + 1] = LOGP ? x2.y : ex.y;
+                    acc[(e / 2) & 1] = add2(acc[(e / 2) & 1], ex);
+                }
+            }
+            const float2 a2 = add2(acc[0], acc[1]);
+            sum = a2.x + a2.y;
+        } else {
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const long vi = threadIdx.x + (long)k * kTmaConsumers;
+                if (vi < nvec) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(srow + vi * V);
+                    if constexpr (V == 8) {
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            v[k][2 * e] = __uint_as_float(w[e] << 16);
+                            v[k][2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+                        }
+                    } else {
+                        v[k][0] = __uint_as_float(u.x); v[k][1] = __uint_as_float(u.y);
+                        v[k][2] = __uint_as_float(u.z); v[k][3] = __uint_as_float(u.w);
                     }
                 } else {
-                    v[k][0] = __uint_as_float(u.x); v[k][1] = __uint_as_float(u.y);
-                    v[k][2] = __uint_as_float(u.z); v[k][3] = __uint_as_float(u.w);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) v[k][e] = -CUDART_INF_F;
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < V; ++e) v[k][e] = -CUDART_INF_F;
             }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty(s));
-        // this thread's (m, s); v becomes exp(v - m) in place
-        float m = -CUDART_INF_F;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(s));
+            m = -CUDART_INF_F;
 #pragma unroll
-        for (int k = 0; k < NV; ++k)
+            for (int k = 0; k < NV; ++k)
 #pragma unroll
-            for (int e = 0; e < V; ++e) m = fmaxf(m, v[k][e]);
-        float sum = 0.f;
-        if (m != -CUDART_INF_F) {
+                for (int e = 0; e < V; ++e) m = fmaxf(m, v[k][e]);
+            const float mk = m == -CUDART_INF_F ? 0.f : m;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < NV; ++k)
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
-                    const float ex = ex2((v[k][e] - m) * kc);
-                    if (WRITE_P && !LOGP) v[k][e] = ex;  // log p keeps x itself
+                    const float ex = ex2((v[k][e] - mk) * kc);
+                    if (WRITE_P && !LOGP) v[k][e] = ex;
                     acc[e & 3] += ex;
                 }
             sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
@@ -705,9 +794,11 @@ bool try_launch_tma(const TIn* X, TOut* P, float* LSE, long rows, long cols, int
         }
         *err = e;
     };
-    if (nvec <= 2L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 2, LOGP>);
-    else if (nvec <= 4L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4, LOGP>);
-    else launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP>);
+    // (rows up to 32 KB always get four stages)
+    if (nvec <= 2L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 2, LOGP, true>);
+    else if (nvec <= 4L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4, LOGP, true>);
+    else if (nst >= 4) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, true>);
+    else launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, false>);
     return true;
 }
 

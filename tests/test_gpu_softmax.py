@@ -92,6 +92,36 @@ def test_pipelined_rows(rows, cols, din, dout):
     assert ok, rel
 
 
+@pytest.mark.parametrize("cols", [40, 1000, 8192, 32768, 100000])
+@pytest.mark.parametrize("din", [torch.bfloat16, torch.float32])
+def test_masked_rows_minus_inf(cols, din):
+    """Masked logits (-inf), as padding masks make them: row r keeps only its
+    first k_r entries (k_r from 1 to cols) and the last row a random tenth.
+    exp(-inf - m) = 0, so p = 0 and log p = -inf there, and LSE is that of
+    the kept entries.  Long masked runs leave whole per-thread slices at -inf."""
+    x = inputs.rows_inputs(8, cols, torch.float32, seed=cols + 5)
+    for r, k in enumerate([1, 3, 100, cols // 3, cols // 2 + 1, cols - 1, cols]):
+        x[r, max(1, min(k, cols)):] = float("-inf")
+    g = torch.Generator().manual_seed(cols)
+    drop = torch.rand(cols, generator=g) < 0.9
+    drop[0] = False
+    x[7, drop] = float("-inf")
+    x = x.to(din)
+    p, lse = fattn.softmax_rows(x.cuda())
+    assert fattn.device_status() == fattn.FA_OK
+    assert not torch.isnan(p).any().item()
+    _check(x, p, lse)
+    lse2 = fattn.logsumexp_rows(x.cuda())
+    ok, rel = lse_ok(to_np(lse2), oracle.logsumexp_rows(x))
+    assert ok, rel
+    y, _ = fattn.log_softmax_rows(x.cuda(), out_dtype=torch.float32)
+    Y, _ = oracle.log_softmax_rows(x)
+    yg = to_np(y)
+    assert np.array_equal(np.isneginf(yg), np.isneginf(Y))
+    fin = np.isfinite(Y)
+    assert np.all(np.abs(yg[fin] - Y[fin]) <= 1e-5 + 1e-6 * np.abs(Y[fin]))
+
+
 def test_many_short_rows():
     x = inputs.rows_inputs(70000, 40, torch.bfloat16, seed=2)
     p, lse = fattn.softmax_rows(x.cuda())
