@@ -11,14 +11,15 @@
 // That form is associative, so per-thread partials merge through warp
 // shuffles and shared memory in any order.
 //
-// Pipelined kernel (rows of 16-64 KB whose byte length is a multiple of 16):
+// Pipelined kernel (rows of 8-64 KB whose byte length is a multiple of 16):
 // persistent, one CTA per SM.  A producer warp streams whole rows into a ring
 // of shared-memory stages with bulk TMA copies (mbarrier-tracked), so several
-// rows are in flight per SM at all times; 16 consumer warps take a row from
-// shared memory into registers (128-bit loads), release the stage, compute
-// exp once per element relative to their own max, merge (m, s) across the
-// CTA and write P with 128-bit coalesced stores.  X is read from HBM once and
-// P written once.
+// rows are in flight per SM at all times; 16 consumer warps (one group, or
+// four groups of 4 taking alternate rows when rows are 16 KB or shorter) take
+// a row from shared memory into registers (128-bit loads), release the stage,
+// compute exp once per element relative to their own max, merge (m, s)
+// across the group and write P with 128-bit coalesced stores.  X is read from
+// HBM once and P written once.
 // Resident kernel (other row lengths up to 64K elements): one CTA per row,
 // each thread holds its slice of the row in registers (NV 16-byte vectors),
 // also one read and one write.
@@ -360,33 +361,41 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_stream(const TIn* __rest
 // ------------------------------------------------------------------ pipelined
 constexpr int kTmaConsumers = 512;                 // 16 consumer warps
 constexpr int kTmaThreads = kTmaConsumers + 32;    // + 1 producer warp
-constexpr int kTmaMaxStages = 4;
+constexpr int kTmaMaxStages = 8;
 constexpr uint32_t kTmaSmemBudget = 200 * 1024;
-constexpr uint32_t kTmaBarBytes = 128;             // full[4], empty[4], red
+constexpr uint32_t kTmaBarBytes = 256;             // full[8], empty[8], red[4]
 constexpr uint32_t kTmaSmemExtra = 128 /* alignment */ + kTmaBarBytes + 2 * 16 * 8 /* (m, s) slots */ + 16;
 
 // One CTA per SM; rows r = blockIdx.x + i * gridDim.x go through a ring of
-// `nst` shared-memory stages of `stage_bytes` each.
+// `nst` shared-memory stages of `stage_bytes` each.  The 16 consumer warps
+// form NG groups; group g takes rows i = g, g + NG, ... (whole rows: 64 KB
+// for one group of 16 warps, 32 KB for two of 8, 16 KB for four of 4), so
+// that one group's cross-warp merge overlaps the others' work on shorter
+// rows.  nst is a multiple of NG: stage s only ever holds rows of group
+// s % NG, which consumes its stages' phases in order.
 // PACKED: the slice stays packed until the exponent pass, which runs on
 // fp32 pairs (faster with four or more stages in the ring; with three, at
 // 64 KB rows, the unpacked form is).
-template <typename TIn, typename TOut, bool WRITE_P, int NV, bool LOGP, bool PACKED>
+template <typename TIn, typename TOut, bool WRITE_P, int NV, bool LOGP, bool PACKED, int NG>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restrict__ LSE, long rows, long cols,
                  uint32_t stage_bytes, int nst, int* status) {
     constexpr int V = Elem<TIn>::kVec;
     constexpr int W = kTmaConsumers / 32;
+    constexpr int WG = W / NG;              // warps per group
+    constexpr int GT = kTmaConsumers / NG;  // threads per group
+    static_assert(NG == 1 || NG == 2 || NG == 4, "consumer groups");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 127u) & ~127u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // after the stages: mbarriers, then the (m, s) slots [2][W], then the abort flag
+    // after the stages: mbarriers, then the (m, s) slots [NG][2][WG], then the abort flag
     const uint32_t bar0 = base + (uint32_t)nst * stage_bytes;
     float2* red = reinterpret_cast<float2*>(gbase + (uint32_t)nst * stage_bytes + kTmaBarBytes);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * W);
     auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
     auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kTmaMaxStages + s); };
-    const uint32_t red_bar = bar0 + 8u * (uint32_t)(2 * kTmaMaxStages);
+    auto red_bar = [&](int g) { return bar0 + 8u * (uint32_t)(2 * kTmaMaxStages + g); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t row_bytes = (uint32_t)(cols * (long)sizeof(TIn));
@@ -395,9 +404,9 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), W);
+            mbar_init(empty(s), WG);  // released by the group that owns the stage
         }
-        mbar_init(red_bar, W);
+        for (int g = 0; g < NG; ++g) mbar_init(red_bar(g), WG);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -433,8 +442,11 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
 
     // ---------------------------------------------------- consumers
     const float kc = kLog2e;
-    long i = 0;
-    for (long r = blockIdx.x; r < rows; r += gridDim.x, ++i) {
+    const int g = NG == 1 ? 0 : warp / WG;                              // consumer group
+    const int gw = NG == 1 ? warp : warp % WG;                          // warp within the group
+    const int gt = NG == 1 ? (int)threadIdx.x : (int)threadIdx.x % GT;  // thread within the group
+    // row i of this CTA is the group's (i / NG)-th
+    for (long i = g, r = blockIdx.x + (long)g * gridDim.x; r < rows; i += NG, r += (long)NG * gridDim.x) {
         const int s = (int)(i % nst);
         const uint32_t ph = (uint32_t)(i / nst) & 1u;
         bool ok = mbar_wait_bounded(full(s), ph, abort_flag, kWaitLimitNs);
@@ -457,7 +469,7 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
             uint4 raw[NV];
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
-                const long vi = threadIdx.x + (long)k * kTmaConsumers;
+                const long vi = gt + (long)k * GT;
                 constexpr uint32_t ni = neg_inf_word<TIn>();
                 raw[k] = vi < nvec ? *reinterpret_cast<const uint4*>(srow + vi * V) : make_uint4(ni, ni, ni, ni);
             }
@@ -490,7 +502,7 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
         } else {
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
-                const long vi = threadIdx.x + (long)k * kTmaConsumers;
+                const long vi = gt + (long)k * GT;
                 if (vi < nvec) {
                     const uint4 u = *reinterpret_cast<const uint4*>(srow + vi * V);
                     if constexpr (V == 8) {
@@ -528,7 +540,7 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
                 }
             sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
-        // merge (m, s): within the warp, then the 16 warps through shared memory
+        // merge (m, s): within the warp, then the group's warps through shared memory
         float M = m, S = sum;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -538,11 +550,11 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
         }
         // (a bounded mbarrier exchange rather than a named barrier, so a warp
         // that gave up can never leave the others waiting forever)
-        float2* slot = red + (i & 1) * W;
-        if (lane == 0) slot[warp] = make_float2(M, S);
+        float2* slot = red + (g * 2 + ((i / NG) & 1)) * WG;
+        if (lane == 0) slot[gw] = make_float2(M, S);
         __syncwarp();
-        if (lane == 0) mbar_arrive(red_bar);
-        ok = mbar_wait_bounded(red_bar, (uint32_t)(i & 1), abort_flag, kWaitLimitNs);
+        if (lane == 0) mbar_arrive(red_bar(g));
+        ok = mbar_wait_bounded(red_bar(g), (uint32_t)((i / NG) & 1), abort_flag, kWaitLimitNs);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) {
             *abort_flag = 1;
@@ -550,11 +562,11 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
             break;
         }
         {
-            const float2 a = slot[lane & (W - 1)];
+            const float2 a = slot[lane & (WG - 1)];
             M = a.x;
             S = a.y;
 #pragma unroll
-            for (int off = W / 2; off > 0; off >>= 1) {
+            for (int off = WG / 2; off > 0; off >>= 1) {
                 const float m2 = __shfl_xor_sync(0xFFFFFFFFu, M, off);
                 const float s2 = __shfl_xor_sync(0xFFFFFFFFu, S, off);
                 merge_ms(M, S, m2, s2);
@@ -567,7 +579,7 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
             TOut* prow = P + r * cols;
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
-                const long vi = threadIdx.x + (long)k * kTmaConsumers;
+                const long vi = gt + (long)k * GT;
                 if (vi < nvec) {
                     float o[V];
 #pragma unroll
@@ -576,7 +588,7 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
                 }
             }
         }
-        if (LSE != nullptr && threadIdx.x == 0) LSE[r] = M + logf(S);
+        if (LSE != nullptr && gt == 0) LSE[r] = M + logf(S);
     }
 }
 
@@ -587,9 +599,10 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
 // ever holds rows of group s % 2 and each group consumes its stages' phases in
 // order (a group can never run a phase ahead on a stage the other group still
 // owns).  A group copies its row slice into registers (packed), releases the
-// stage, then folds the values into a running (m, s) four vectors at a time
-// (the online normaliser applied per chunk).
+// stage, takes the slice max on the packed values and sums one exponential
+// per element relative to it.
 constexpr int kLseGroups = 2;
+constexpr int kLseMaxStages = 4;
 constexpr int kLseGroupThreads = kTmaConsumers / kLseGroups;  // 256
 
 template <typename TIn, int NV>
@@ -779,11 +792,16 @@ bool try_launch_tma(const TIn* X, TOut* P, float* LSE, long rows, long cols, int
                     cudaError_t* err) {
     constexpr int V = Elem<TIn>::kVec;
     const long row_bytes = cols * (long)sizeof(TIn);
-    if (cols % V != 0 || row_bytes < 16384 || row_bytes > 65536 || rows < 64) return false;
+    if (cols % V != 0 || row_bytes < 8192 || row_bytes > 65536 || rows < 64) return false;
     const long nvec = cols / V;
+    // consumer groups: one for rows above 16 KB, four (of 4 warps) up to 16 KB
+    const int ng = row_bytes > 16384 ? 1 : 4;
     const uint32_t stage = (uint32_t)((row_bytes + 127) / 128 * 128);
+    // (one group: at most four stages, as measured best; four groups: two each)
+    const int max_st = ng == 1 ? 4 : kTmaMaxStages;
     int nst = (int)(kTmaSmemBudget / stage);
-    nst = nst > kTmaMaxStages ? kTmaMaxStages : nst;
+    nst = nst > max_st ? max_st : nst;
+    nst -= nst % ng;  // stage s belongs to group s % ng
     const uint32_t smem = (uint32_t)nst * stage + kTmaSmemExtra;
     const long grid = rows < device_sms() ? rows : device_sms();
     auto launch = [&](auto kern) {
@@ -794,11 +812,16 @@ bool try_launch_tma(const TIn* X, TOut* P, float* LSE, long rows, long cols, int
         }
         *err = e;
     };
-    // (rows up to 32 KB always get four stages)
-    if (nvec <= 2L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 2, LOGP, true>);
-    else if (nvec <= 4L * kTmaConsumers) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4, LOGP, true>);
-    else if (nst >= 4) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, true>);
-    else launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, false>);
+    if (ng == 4) {
+        if (nvec <= 4L * (kTmaConsumers / 4)) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4, LOGP, true, 4>);
+        else launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, true, 4>);
+    } else if (nvec <= 4L * kTmaConsumers) {  // up to 32 KB: four stages
+        launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4, LOGP, true, 1>);
+    } else if (nst >= 4) {
+        launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, true, 1>);
+    } else {
+        launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, false, 1>);
+    }
     return true;
 }
 
@@ -815,7 +838,7 @@ bool try_launch_lse_tma(const TIn* X, float* LSE, long rows, long cols, int* sta
     const long nvec = cols / V;
     const uint32_t stage = (uint32_t)((row_bytes + 127) / 128 * 128);
     int nst = (int)(kTmaSmemBudget / stage);
-    nst = nst > kTmaMaxStages ? kTmaMaxStages : nst;
+    nst = nst > kLseMaxStages ? kLseMaxStages : nst;
     nst &= ~1;  // even: stage s belongs to consumer group s % 2
     const uint32_t smem = (uint32_t)nst * stage + kTmaSmemExtra;
     const long grid = rows < device_sms() ? rows : device_sms();
