@@ -601,24 +601,24 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
 // owns).  A group copies its row slice into registers (packed), releases the
 // stage, takes the slice max on the packed values and sums one exponential
 // per element relative to it.
-constexpr int kLseGroups = 2;
-constexpr int kLseMaxStages = 4;
-constexpr int kLseGroupThreads = kTmaConsumers / kLseGroups;  // 256
-
-template <typename TIn, int NV>
+// NG consumer groups: two of 8 warps for rows above 16 KB, four of 4 warps for
+// rows of 8-16 KB.
+template <typename TIn, int NV, int NG>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows, long cols, uint32_t stage_bytes,
                    int nst, int* status, const long long* __restrict__ labels, float* __restrict__ loss) {
     constexpr int V = Elem<TIn>::kVec;
-    constexpr int WG = kLseGroupThreads / 32;  // warps per group
+    constexpr int GT = kTmaConsumers / NG;     // threads per group
+    constexpr int WG = GT / 32;                // warps per group
+    static_assert(NG == 2 || NG == 4, "consumer groups");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 127u) & ~127u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // after the stages: full[4], empty[4], red[2]; then (m, s) slots [group][2][WG]; then the abort flag
+    // after the stages: full[8], empty[8], red[NG]; then (m, s) slots [group][2][WG]; then the abort flag
     const uint32_t bar0 = base + (uint32_t)nst * stage_bytes;
     float2* red = reinterpret_cast<float2*>(gbase + (uint32_t)nst * stage_bytes + kTmaBarBytes);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kLseGroups * 2 * WG);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + NG * 2 * WG);
     auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
     auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kTmaMaxStages + s); };
     auto red_bar = [&](int g) { return bar0 + 8u * (uint32_t)(2 * kTmaMaxStages + g); };
@@ -631,7 +631,7 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
             mbar_init(full(s), 1);
             mbar_init(empty(s), WG);  // released by the group that owns the stage
         }
-        for (int g = 0; g < kLseGroups; ++g) mbar_init(red_bar(g), WG);
+        for (int g = 0; g < NG; ++g) mbar_init(red_bar(g), WG);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -665,10 +665,10 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
 
     const int g = warp / WG;                        // consumer group
     const int gw = warp % WG;                       // warp within the group
-    const int gt = threadIdx.x % kLseGroupThreads;  // thread within the group
+    const int gt = threadIdx.x % GT;                // thread within the group
     const float2 cc = make_float2(kLog2e, kLog2e);
     long k = 0;                                     // rows this group has done
-    for (long i = g; blockIdx.x + i * (long)gridDim.x < rows; i += kLseGroups, ++k) {
+    for (long i = g; blockIdx.x + i * (long)gridDim.x < rows; i += NG, ++k) {
         const long r = blockIdx.x + i * (long)gridDim.x;
         const int s = (int)(i % nst);
         const uint32_t ph = (uint32_t)(i / nst) & 1u;
@@ -685,7 +685,7 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
         uint4 raw[NV];
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
-            const long vi = gt + (long)kk * kLseGroupThreads;
+            const long vi = gt + (long)kk * GT;
             // (past the row end: -inf, which neither the max nor the sum sees)
             constexpr uint32_t ni = neg_inf_word<TIn>();
             raw[kk] = vi < nvec ? *reinterpret_cast<const uint4*>(srow + vi * V) : make_uint4(ni, ni, ni, ni);
@@ -832,14 +832,16 @@ bool try_launch_lse_tma(const TIn* X, float* LSE, long rows, long cols, int* sta
                         cudaError_t* err, const long long* labels, float* loss) {
     constexpr int V = Elem<TIn>::kVec;
     const long row_bytes = cols * (long)sizeof(TIn);
-    // (rows of 16 KB and less: one 128-thread CTA per row streams them faster,
-    // 16384 x 8192 bf16 in 71.8 us against 84.2 here)
-    if (cols % V != 0 || row_bytes <= 16384 || row_bytes > 65536 || rows < 64) return false;
+    if (cols % V != 0 || row_bytes < 8192 || row_bytes > 65536 || rows < 64) return false;
     const long nvec = cols / V;
+    // consumer groups: two above 16 KB (at most four stages), four up to 16 KB
+    // (eight stages, two per group)
+    const int ng = row_bytes > 16384 ? 2 : 4;
+    const int max_st = ng == 2 ? 4 : kTmaMaxStages;
     const uint32_t stage = (uint32_t)((row_bytes + 127) / 128 * 128);
     int nst = (int)(kTmaSmemBudget / stage);
-    nst = nst > kLseMaxStages ? kLseMaxStages : nst;
-    nst &= ~1;  // even: stage s belongs to consumer group s % 2
+    nst = nst > max_st ? max_st : nst;
+    nst -= nst % ng;  // stage s belongs to consumer group s % ng
     const uint32_t smem = (uint32_t)nst * stage + kTmaSmemExtra;
     const long grid = rows < device_sms() ? rows : device_sms();
     auto launch = [&](auto kern) {
@@ -850,8 +852,14 @@ bool try_launch_lse_tma(const TIn* X, float* LSE, long rows, long cols, int* sta
         }
         *err = e;
     };
-    if (nvec <= 8L * kLseGroupThreads) launch(logsumexp_rows_tma<TIn, 8>);
-    else launch(logsumexp_rows_tma<TIn, 16>);
+    if (ng == 4) {
+        if (nvec <= 4L * (kTmaConsumers / 4)) launch(logsumexp_rows_tma<TIn, 4, 4>);
+        else launch(logsumexp_rows_tma<TIn, 8, 4>);
+    } else if (nvec <= 8L * (kTmaConsumers / 2)) {
+        launch(logsumexp_rows_tma<TIn, 8, 2>);
+    } else {
+        launch(logsumexp_rows_tma<TIn, 16, 2>);
+    }
     return true;
 }
 
