@@ -615,7 +615,7 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 127u) & ~127u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // after the stages: full[8], empty[8], red[NG]; then (m, s) slots [group][2][WG]; then the abort flag
+    // after the stages: full[], empty[] (kTmaMaxStages each), red[NG]; then (m, s) slots [group][2][WG]; then the abort flag
     const uint32_t bar0 = base + (uint32_t)nst * stage_bytes;
     float2* red = reinterpret_cast<float2*>(gbase + (uint32_t)nst * stage_bytes + kTmaBarBytes);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(red + NG * 2 * WG);
