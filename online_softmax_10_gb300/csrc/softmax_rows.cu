@@ -20,6 +20,9 @@
 // compute exp once per element relative to their own max, merge (m, s)
 // across the group and write P with 128-bit coalesced stores.  X is read from
 // HBM once and P written once.
+// Warp-per-row kernel (rows of whole 16-byte vectors up to 4 KB, 8 KB for
+// log-sum-exp only): persistent warps, the next row loaded while the current
+// one is reduced.
 // Resident kernel (other row lengths up to 64K elements): one CTA per row,
 // each thread holds its slice of the row in registers (NV 16-byte vectors),
 // also one read and one write.
@@ -863,6 +866,137 @@ bool try_launch_lse_tma(const TIn* X, float* LSE, long rows, long cols, int* sta
     return true;
 }
 
+// ------------------------------------------------------------------ warp per row
+// Rows of at most 256 16-byte vectors (4 KB; 8 KB for log-sum-exp only): one
+// warp per row, persistent over rows, with the next row's slice loaded while
+// the current one is reduced.  The whole row is in the warp's registers, so
+// the row max is known before any exponential and the sum is taken once
+// against it: pass 1 the max (bf16: on the packed pairs), pass 2
+// S = sum exp(x - M), pass 3 (with P) p = 2^((x - M) log2 e - log2 S) or
+// log p = x - (M + ln S).
+// KIND: 0 softmax (P, LSE), 1 log-softmax (log p, LSE), 2 log-sum-exp only
+// (LSE and / or the fused cross-entropy loss).
+constexpr int kWarpRowThreads = 256;
+
+template <typename TIn, int NV>
+__device__ __forceinline__ void warp_row_load(const TIn* __restrict__ X, long row, long rows, long cols, long nvec,
+                                              int lane, uint4* buf) {
+    constexpr int V = Elem<TIn>::kVec;
+    constexpr uint32_t ni = neg_inf_word<TIn>();
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const long vi = lane + 32L * k;
+        buf[k] = (row < rows && vi < nvec) ? __ldg(reinterpret_cast<const uint4*>(X + row * cols + vi * V))
+                                           : make_uint4(ni, ni, ni, ni);
+    }
+}
+
+// The 2 (bf16) or 1 (fp32) values of packed word e of a vector as floats.
+template <typename TIn>
+__device__ __forceinline__ float2 unpack_pair(const uint4& u, int e) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    if constexpr (sizeof(TIn) == 2) {
+        return make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+    } else {
+        return make_float2(__uint_as_float(w[2 * e]), __uint_as_float(w[2 * e + 1]));  // e < 2
+    }
+}
+
+template <typename TIn, typename TOut, int NV, int KIND>
+__global__ void __launch_bounds__(kWarpRowThreads)
+softmax_rows_warp(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restrict__ LSE, long rows, long cols,
+                  const long long* __restrict__ labels, float* __restrict__ loss) {
+    constexpr int V = Elem<TIn>::kVec;
+    constexpr int NP = V / 2;  // float pairs per vector
+    const long nvec = cols / V;
+    const int lane = threadIdx.x & 31;
+    const long nwarps = ((long)gridDim.x * kWarpRowThreads) >> 5;
+    long row = ((long)blockIdx.x * kWarpRowThreads + threadIdx.x) >> 5;
+    uint4 cur[NV], nxt[NV];
+    warp_row_load<TIn, NV>(X, row, rows, cols, nvec, lane, cur);
+    for (; row < rows; row += nwarps) {
+        warp_row_load<TIn, NV>(X, row + nwarps, rows, cols, nvec, lane, nxt);
+        // pass 1: the row max
+        float M = slice_max<TIn, NV>(cur);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+        // pass 2: S = sum exp(x - M)  (a row of -inf only: M taken as 0, S = 0)
+        const float Mk = M == -CUDART_INF_F ? 0.f : M;
+        const float2 mm = make_float2(Mk, Mk), kk2 = make_float2(kLog2e, kLog2e);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < NP; ++e) {
+                const float2 t2 = mul2(sub2(unpack_pair<TIn>(cur[k], e), mm), kk2);
+                acc = add2(acc, make_float2(ex2(t2.x), ex2(t2.y)));
+            }
+        float S = acc.x + acc.y;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, off);
+        const float lse = M + logf(S);
+        if constexpr (KIND != 2) {
+            // pass 3: p (or log p), 16-byte stores
+            const float l2s = __log2f(S);
+            TOut* prow = P + row * cols;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const long vi = lane + 32L * k;
+                if (vi < nvec) {
+                    float o[V];
+#pragma unroll
+                    for (int e = 0; e < NP; ++e) {
+                        const float2 x2 = unpack_pair<TIn>(cur[k], e);
+                        if constexpr (KIND == 1) {
+                            o[2 * e] = x2.x - lse;
+                            o[2 * e + 1] = x2.y - lse;
+                        } else {
+                            o[2 * e] = ex2(fmaf(x2.x - Mk, kLog2e, -l2s));
+                            o[2 * e + 1] = ex2(fmaf(x2.y - Mk, kLog2e, -l2s));
+                        }
+                    }
+                    store_out<TOut, V>(prow + vi * V, o, true, V);
+                }
+            }
+        }
+        if (lane == 0) {
+            if constexpr (KIND == 2) write_row_lse(X, row, cols, lse, LSE, labels, loss);
+            else if (LSE != nullptr) LSE[row] = lse;
+        }
+#pragma unroll
+        for (int k = 0; k < NV; ++k) cur[k] = nxt[k];
+    }
+}
+
+// Launch the warp-per-row kernel for rows of whole 16-byte vectors, at most
+// 256 (512 for log-sum-exp only, which keeps no third pass).
+template <typename TIn, typename TOut, int KIND>
+bool try_launch_warp_rows(const TIn* X, TOut* P, float* LSE, long rows, long cols, cudaStream_t st, cudaError_t* err,
+                          const long long* labels = nullptr, float* loss = nullptr) {
+    constexpr int V = Elem<TIn>::kVec;
+    const long nvec = cols / V;
+    if (cols % V != 0 || nvec > (KIND == 2 ? 512 : 256)) return false;
+    const long want = (rows + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32);
+    auto launch = [&](auto kern) {
+        // persistent: as many CTAs as fit on the GPU at once, or fewer for few rows
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarpRowThreads, 0);
+        if (e == cudaSuccess) {
+            const long cap = (long)(per_sm > 0 ? per_sm : 1) * device_sms();
+            const long grid = want < cap ? want : cap;
+            kern<<<(unsigned)grid, kWarpRowThreads, 0, st>>>(X, P, LSE, rows, cols, labels, loss);
+            e = cudaGetLastError();
+        }
+        *err = e;
+    };
+    if (nvec <= 32) launch(softmax_rows_warp<TIn, TOut, 1, KIND>);
+    else if (nvec <= 64) launch(softmax_rows_warp<TIn, TOut, 2, KIND>);
+    else if (nvec <= 128) launch(softmax_rows_warp<TIn, TOut, 4, KIND>);
+    else if (nvec <= 256) launch(softmax_rows_warp<TIn, TOut, 8, KIND>);
+    else if constexpr (KIND == 2) launch(softmax_rows_warp<TIn, TOut, 16, KIND>);
+    return true;
+}
+
 long grid_for_rows(long rows) {
     const long kMaxGrid = 1L << 30;
     return rows < kMaxGrid ? rows : kMaxGrid;
@@ -874,6 +1008,7 @@ cudaError_t softmax_dispatch(const TIn* X, TOut* P, float* LSE, long rows, long 
     constexpr int V = Elem<TIn>::kVec;
     cudaError_t terr;
     if (try_launch_tma<TIn, TOut, true, LOGP>(X, P, LSE, rows, cols, status, st, &terr)) return terr;
+    if (try_launch_warp_rows<TIn, TOut, LOGP ? 1 : 0>(X, P, LSE, rows, cols, st, &terr)) return terr;
     const int vec_ok = (cols % V) == 0;
     const long nvec = (cols + V - 1) / V;
     const dim3 grid((unsigned)grid_for_rows(rows));
@@ -897,6 +1032,7 @@ cudaError_t lse_dispatch(const TIn* X, float* LSE, long rows, long cols, int* st
                          const long long* labels, float* loss) {
     constexpr int V = Elem<TIn>::kVec;
     cudaError_t terr;
+    if (try_launch_warp_rows<TIn, float, 2>(X, nullptr, LSE, rows, cols, st, &terr, labels, loss)) return terr;
     if (try_launch_lse_tma<TIn>(X, LSE, rows, cols, status, st, &terr, labels, loss)) return terr;
     const int vec_ok = (cols % V) == 0;
     const long nvec = (cols + V - 1) / V;

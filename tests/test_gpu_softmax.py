@@ -122,6 +122,28 @@ def test_masked_rows_minus_inf(cols, din):
     assert np.all(np.abs(yg[fin] - Y[fin]) <= 1e-5 + 1e-6 * np.abs(Y[fin]))
 
 
+@pytest.mark.parametrize("cols,din", [(1024, torch.bfloat16), (2048, torch.bfloat16), (4096, torch.bfloat16),
+                                      (1024, torch.float32), (520, torch.float32)])
+def test_many_rows_per_warp(cols, din):
+    """More rows than resident warps: rows of up to 4 KB (8 KB for the LSE
+    alone) go to one warp per row, each warp looping over rows with the next
+    row loaded ahead; a seeded sample of rows against the oracle."""
+    rows = 6000
+    x = inputs.rows_inputs(rows, cols, din, seed=cols + 11)
+    p, lse = fattn.softmax_rows(x.cuda())
+    lse2 = fattn.logsumexp_rows(x.cuda())
+    y, _ = fattn.log_softmax_rows(x.cuda(), out_dtype=torch.float32)
+    assert fattn.device_status() == fattn.FA_OK
+    sample = inputs.sample_rows(rows, 64, seed=cols).numpy()
+    _check(x, p, lse, sample)
+    sub = x[torch.as_tensor(sample)]
+    ok, rel = lse_ok(to_np(lse2)[sample], oracle.logsumexp_rows(sub))
+    assert ok, rel
+    Y, _ = oracle.log_softmax_rows(sub)
+    yg = to_np(y)[sample]
+    assert np.all(np.abs(yg - Y) <= 1e-5 + 1e-6 * np.abs(Y)), float(np.max(np.abs(yg - Y)))
+
+
 def test_many_short_rows():
     x = inputs.rows_inputs(70000, 40, torch.bfloat16, seed=2)
     p, lse = fattn.softmax_rows(x.cuda())
