@@ -171,6 +171,17 @@ __device__ __forceinline__ float slice_max(const uint4* raw) {
     }
 }
 
+// Float pair e of a packed 16-byte vector: bf16 word e, or fp32 words 2e, 2e + 1.
+template <typename TIn>
+__device__ __forceinline__ float2 unpack_pair(const uint4& u, int e) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    if constexpr (sizeof(TIn) == 2) {
+        return make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+    } else {
+        return make_float2(__uint_as_float(w[2 * e]), __uint_as_float(w[2 * e + 1]));  // e < 2
+    }
+}
+
 // (m, s) <- (m, s) (+) (m2, s2): the pairwise online-normaliser update.
 // Sums are relative to their own max; an empty partial is (-inf, 0).
 __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
@@ -219,46 +230,87 @@ __device__ __forceinline__ void block_merge(float& m, float& s, float* sm_m, flo
     }
 }
 
-// One CTA per row (grid-strided); the row lives in registers.
+// 16-byte vector vi of a row as packed words; elements past the row end (or
+// the whole vector, when the row is not a whole number of vectors and this
+// one is cut) are read one at a time, missing ones as -inf.
+template <typename TIn>
+__device__ __forceinline__ uint4 load_vec_packed(const TIn* __restrict__ x, long e0, long cols, bool vec_ok) {
+    constexpr int V = Elem<TIn>::kVec;
+    if (vec_ok && e0 + V <= cols) return __ldg(reinterpret_cast<const uint4*>(x + e0));
+    uint32_t w[4];
+    if constexpr (sizeof(TIn) == 2) {
+        const unsigned short* xs = reinterpret_cast<const unsigned short*>(x);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = e0 + 2 * i < cols ? __ldg(xs + e0 + 2 * i) : 0xFF80u;
+            const uint32_t hi = e0 + 2 * i + 1 < cols ? __ldg(xs + e0 + 2 * i + 1) : 0xFF80u;
+            w[i] = lo | (hi << 16);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = e0 + i < cols ? __float_as_uint(__ldg(x + e0 + i)) : 0xFF800000u;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Block-wide max or sum of one float per thread; every thread gets the result.
+template <int THREADS, bool MAX>
+__device__ __forceinline__ float block_reduce(float v, float* sm) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        v = MAX ? fmaxf(v, o) : v + o;
+    }
+    if constexpr (THREADS > 32) {
+        constexpr int W = THREADS / 32;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (lane == 0) sm[warp] = v;
+        __syncthreads();
+        v = lane < W ? sm[lane] : (MAX ? -CUDART_INF_F : 0.f);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, v, off);
+            v = MAX ? fmaxf(v, o) : v + o;
+        }
+        __syncthreads();  // the scratch may be reused next
+    }
+    return v;
+}
+
+// One CTA per row (grid-strided); the row lives in registers, packed.  Its
+// max first (block-wide), then S = sum exp(x - M) (block-wide), then
+// p = 2^((x - M) log2 e - log2 S) or log p = x - (M + ln S): the three passes
+// of the safe softmax over registers, one read and one write of the row.
 template <typename TIn, typename TOut, int THREADS, int NV, bool LOGP>
 __global__ void __launch_bounds__(THREADS) softmax_rows_resident(const TIn* __restrict__ X, TOut* __restrict__ P,
                                                                  float* __restrict__ LSE, long rows, long cols,
                                                                  int vec_ok) {
     constexpr int V = Elem<TIn>::kVec;
-    __shared__ float sm_m[32], sm_s[32];
+    constexpr int NP = V / 2;
+    __shared__ float sm[32];
     for (long row = blockIdx.x; row < rows; row += gridDim.x) {
         const TIn* x = X + row * cols;
-        float v[NV][V];
-        // one read of the row: 16-byte vectors, consecutive threads adjacent
+        uint4 raw[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const long e0 = (long)(threadIdx.x + k * THREADS) * V;
-            if (vec_ok && e0 + V <= cols) {
-                Elem<TIn>::loadv(x + e0, v[k]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < V; ++i) v[k][i] = (e0 + i < cols) ? Elem<TIn>::load1(x + e0 + i) : -CUDART_INF_F;
-            }
+            constexpr uint32_t ni = neg_inf_word<TIn>();
+            raw[k] = e0 < cols ? load_vec_packed<TIn>(x, e0, cols, vec_ok != 0) : make_uint4(ni, ni, ni, ni);
         }
-        // this thread's (m, s): its max, then the sum of exp relative to it
-        float m = -CUDART_INF_F;
+        const float M = block_reduce<THREADS, true>(slice_max<TIn, NV>(raw), sm);
+        const float Mk = M == -CUDART_INF_F ? 0.f : M;  // a row of -inf only: S = 0
+        const float2 mm = make_float2(Mk, Mk), kk2 = make_float2(kLog2e, kLog2e);
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < NV; ++k)
 #pragma unroll
-            for (int i = 0; i < V; ++i) m = fmaxf(m, v[k][i]);
-        float s = 0.f;
-        if (m != -CUDART_INF_F) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int k = 0; k < NV; ++k)
-#pragma unroll
-                for (int i = 0; i < V; ++i) acc[i & 3] += ex2((v[k][i] - m) * kLog2e);
-            s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-        }
-        block_merge<THREADS>(m, s, sm_m, sm_s);
-        // p = exp(x - M) / S = 2^((x - M) log2e - log2 S);  log p = x - (M + ln S)
-        const float l2s = __log2f(s);
-        const float lse_row = m + logf(s);
+            for (int e = 0; e < NP; ++e) {
+                const float2 t2 = mul2(sub2(unpack_pair<TIn>(raw[k], e), mm), kk2);
+                acc = add2(acc, make_float2(ex2(t2.x), ex2(t2.y)));
+            }
+        const float S = block_reduce<THREADS, false>(acc.x + acc.y, sm);
+        const float l2s = __log2f(S);
+        const float lse_row = M + logf(S);
         TOut* p = P + row * cols;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -266,49 +318,65 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_resident(const TIn* __re
             if (e0 < cols) {
                 float o[V];
 #pragma unroll
-                for (int i = 0; i < V; ++i) o[i] = LOGP ? v[k][i] - lse_row : ex2(fmaf(v[k][i] - m, kLog2e, -l2s));
+                for (int e = 0; e < NP; ++e) {
+                    const float2 x2 = unpack_pair<TIn>(raw[k], e);
+                    o[2 * e] = LOGP ? x2.x - lse_row : ex2(fmaf(x2.x - Mk, kLog2e, -l2s));
+                    o[2 * e + 1] = LOGP ? x2.y - lse_row : ex2(fmaf(x2.y - Mk, kLog2e, -l2s));
+                }
                 const int valid = (int)((cols - e0) < V ? (cols - e0) : V);
                 store_out<TOut, V>(p + e0, o, vec_ok && valid == V, valid);
             }
         }
-        if (LSE != nullptr && threadIdx.x == 0) LSE[row] = m + logf(s);
+        if (LSE != nullptr && threadIdx.x == 0) LSE[row] = lse_row;
+    }
+}
+
+// U strided 16-byte vectors of a row, packed (past the row end: -inf).
+template <typename TIn, int THREADS, int U>
+__device__ __forceinline__ void load_block_packed(const TIn* __restrict__ x, long base, long nvec, long cols,
+                                                  bool vec_ok, uint4* buf) {
+    constexpr int V = Elem<TIn>::kVec;
+    constexpr uint32_t ni = neg_inf_word<TIn>();
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const long vi = base + (long)u * THREADS;
+        buf[u] = vi < nvec ? load_vec_packed<TIn>(x, vi * V, cols, vec_ok) : make_uint4(ni, ni, ni, ni);
     }
 }
 
 // Per-thread online (m, s) over a strided range of 16-byte vectors of a row:
-// U vectors are loaded before they are folded in, for memory-level parallelism.
+// blocks of U vectors, the next block loaded while the current one is folded
+// in (s <- s 2^(m - m') + sum 2^(x - m'), m' = max(m, block max)).
 template <typename TIn, int THREADS, int U>
 __device__ __forceinline__ void row_online_ms(const TIn* __restrict__ x, long cols, bool vec_ok, float& m, float& s) {
     constexpr int V = Elem<TIn>::kVec;
+    constexpr int NP = V / 2;
+    constexpr long STEP = (long)THREADS * U;
     const long nvec = (cols + V - 1) / V;
     m = -CUDART_INF_F;
     s = 0.f;
-    for (long base = threadIdx.x; base < nvec; base += (long)THREADS * U) {
-        float v[U][V];
+    uint4 cur[U], nxt[U];
+    long base = threadIdx.x;
+    load_block_packed<TIn, THREADS, U>(x, base, nvec, cols, vec_ok, cur);
+    for (; base < nvec; base += STEP) {
+        load_block_packed<TIn, THREADS, U>(x, base + STEP, nvec, cols, vec_ok, nxt);
+        const float bm = slice_max<TIn, U>(cur);
+        if (bm != -CUDART_INF_F) {
+            const float mn = fmaxf(m, bm);
+            const float2 mm = make_float2(mn, mn), kk2 = make_float2(kLog2e, kLog2e);
+            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const long e0 = (base + (long)u * THREADS) * V;
-            if (vec_ok && e0 + V <= cols) {
-                Elem<TIn>::loadv(x + e0, v[u]);
-            } else {
+            for (int u = 0; u < U; ++u)
 #pragma unroll
-                for (int i = 0; i < V; ++i) v[u][i] = (e0 + i < cols) ? Elem<TIn>::load1(x + e0 + i) : -CUDART_INF_F;
-            }
+                for (int e = 0; e < NP; ++e) {
+                    const float2 t2 = mul2(sub2(unpack_pair<TIn>(cur[u], e), mm), kk2);
+                    acc = add2(acc, make_float2(ex2(t2.x), ex2(t2.y)));
+                }
+            s = s * ex2((m - mn) * kLog2e) + (acc.x + acc.y);  // m = -inf on the first block: 2^-inf = 0
+            m = mn;
         }
-        float bm = -CUDART_INF_F;
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int i = 0; i < V; ++i) bm = fmaxf(bm, v[u][i]);
-        if (bm == -CUDART_INF_F) continue;
-        const float mn = fmaxf(m, bm);
-        float acc = 0.f;
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int i = 0; i < V; ++i) acc += ex2((v[u][i] - mn) * kLog2e);
-        s = s * ex2((m - mn) * kLog2e) + acc;  // m = -inf on the first block: 2^-inf = 0
-        m = mn;
+        for (int u = 0; u < U; ++u) cur[u] = nxt[u];
     }
 }
 
@@ -343,18 +411,26 @@ __global__ void __launch_bounds__(THREADS) softmax_rows_stream(const TIn* __rest
         const float lse_row = m + logf(s);
         TOut* p = P + row * cols;
         const long nvec = (cols + V - 1) / V;
-        for (long vi = threadIdx.x; vi < nvec; vi += THREADS) {
-            const long e0 = vi * V;
-            float f[V];
-            const int valid = (int)((cols - e0) < V ? (cols - e0) : V);
-            if (vec_ok && valid == V) {
-                Elem<TIn>::loadv(x + e0, f);
-            } else {
-                for (int i = 0; i < V; ++i) f[i] = i < valid ? Elem<TIn>::load1(x + e0 + i) : 0.f;
-            }
+        // second read of the row, U vectors in flight per thread
+        for (long base = threadIdx.x; base < nvec; base += (long)THREADS * U) {
+            uint4 raw[U];
+            load_block_packed<TIn, THREADS, U>(x, base, nvec, cols, vec_ok != 0, raw);
 #pragma unroll
-            for (int i = 0; i < V; ++i) f[i] = LOGP ? f[i] - lse_row : ex2(fmaf(f[i] - m, kLog2e, -l2s));
-            store_out<TOut, V>(p + e0, f, vec_ok && valid == V, valid);
+            for (int u = 0; u < U; ++u) {
+                const long vi = base + (long)u * THREADS;
+                if (vi < nvec) {
+                    const long e0 = vi * V;
+                    float o[V];
+#pragma unroll
+                    for (int e = 0; e < V / 2; ++e) {
+                        const float2 x2 = unpack_pair<TIn>(raw[u], e);
+                        o[2 * e] = LOGP ? x2.x - lse_row : ex2(fmaf(x2.x - m, kLog2e, -l2s));
+                        o[2 * e + 1] = LOGP ? x2.y - lse_row : ex2(fmaf(x2.y - m, kLog2e, -l2s));
+                    }
+                    const int valid = (int)((cols - e0) < V ? (cols - e0) : V);
+                    store_out<TOut, V>(p + e0, o, vec_ok && valid == V, valid);
+                }
+            }
         }
         if (LSE != nullptr && threadIdx.x == 0) LSE[row] = m + logf(s);
     }
@@ -891,17 +967,6 @@ __device__ __forceinline__ void warp_row_load(const TIn* __restrict__ X, long ro
     }
 }
 
-// The 2 (bf16) or 1 (fp32) values of packed word e of a vector as floats.
-template <typename TIn>
-__device__ __forceinline__ float2 unpack_pair(const uint4& u, int e) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    if constexpr (sizeof(TIn) == 2) {
-        return make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
-    } else {
-        return make_float2(__uint_as_float(w[2 * e]), __uint_as_float(w[2 * e + 1]));  // e < 2
-    }
-}
-
 template <typename TIn, typename TOut, int NV, int KIND>
 __global__ void __launch_bounds__(kWarpRowThreads)
 softmax_rows_warp(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restrict__ LSE, long rows, long cols,
@@ -1021,8 +1086,7 @@ cudaError_t softmax_dispatch(const TIn* X, TOut* P, float* LSE, long rows, long 
     else if (nvec <= 1024) FA_RESIDENT(128, 8);
     else if (nvec <= 2048) FA_RESIDENT(256, 8);
     else if (nvec <= 4096) FA_RESIDENT(512, 8);
-    else if (nvec <= 8192) FA_RESIDENT(1024, 8);
-    else softmax_rows_stream<TIn, TOut, 512, 4, LOGP><<<grid, 512, 0, st>>>(X, P, LSE, rows, cols, vec_ok);
+    else softmax_rows_stream<TIn, TOut, 512, 8, LOGP><<<grid, 512, 0, st>>>(X, P, LSE, rows, cols, vec_ok);
 #undef FA_RESIDENT
     return cudaGetLastError();
 }
@@ -1039,7 +1103,7 @@ cudaError_t lse_dispatch(const TIn* X, float* LSE, long rows, long cols, int* st
     const dim3 grid((unsigned)grid_for_rows(rows));
     if (nvec <= 128) logsumexp_rows_stream<TIn, 32, 4><<<grid, 32, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
     else if (nvec <= 1024) logsumexp_rows_stream<TIn, 128, 4><<<grid, 128, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
-    else logsumexp_rows_stream<TIn, 512, 4><<<grid, 512, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
+    else logsumexp_rows_stream<TIn, 512, 8><<<grid, 512, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
     return cudaGetLastError();
 }
 
