@@ -1103,7 +1103,7 @@ cudaError_t lse_dispatch(const TIn* X, float* LSE, long rows, long cols, int* st
     const dim3 grid((unsigned)grid_for_rows(rows));
     if (nvec <= 128) logsumexp_rows_stream<TIn, 32, 4><<<grid, 32, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
     else if (nvec <= 1024) logsumexp_rows_stream<TIn, 128, 4><<<grid, 128, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
-    else logsumexp_rows_stream<TIn, 512, 8><<<grid, 512, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
+    else logsumexp_rows_stream<TIn, 256, 8><<<grid, 256, 0, st>>>(X, LSE, rows, cols, vec_ok, labels, loss);
     return cudaGetLastError();
 }
 
