@@ -32,8 +32,9 @@ def _edge_and_sample(total, count, seed):
     return np.array(sorted(rows))
 
 
-# (rows, cols): the pipelined kernel (64 KB rows), the one-CTA-per-row kernel
-# (8 KB rows) and the streaming kernel (> 64K columns), each past 2^31 elements
+# (rows, cols), each past 2^31 elements: the pipelined kernel (64 KB rows; 8 KB
+# rows with four consumer groups, whose LSE alone takes the warp-per-row
+# kernel) and the streaming kernels (> 64K columns)
 ROW_SHAPES = [(65600, 32768), (525000, 4096), (21500, 100000)]
 
 
