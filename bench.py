@@ -188,6 +188,74 @@ def time_launches(fn, steps: int, warmup: int, world_size: int):
     return max_over_ranks(total, world_size, device="cuda"), per
 
 
+def time_for(fn, seconds: float, warmup: int = 3, flush=None, max_launches: int = 20000):
+    """Mean device seconds per fn() call over about `seconds` of launches,
+    each bracketed by its own pair of CUDA events on the current stream
+    (`flush`, if given, runs between launches outside the events).
+    Returns (mean seconds per launch, launches)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    est = max(a.elapsed_time(b) / 1e3, 1e-6)
+    n = int(max(10, min(max_launches, math.ceil(seconds / est))))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for x, y in evs:
+        if flush is not None:
+            flush()
+        x.record(stream)
+        fn()
+        y.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(x.elapsed_time(y) for x, y in evs) / 1e3, n
+
+
+def link_bandwidth(host_in, dev_in, host_out, dev_out, reps: int = 5):
+    """Pinned host <-> device copy rates on the tensors one end-to-end step
+    moves (one cudaMemcpyAsync per tensor): host-to-device alone,
+    device-to-host alone, and both directions at once on two streams.
+    Returns a dict of GB/s and the both-ways time of one step's copies."""
+    import torch
+    up = torch.cuda.Stream()
+    down = torch.cuda.Stream()
+    bi = sum(t.numel() * t.element_size() for t in host_in)
+    bo = sum(t.numel() * t.element_size() for t in host_out)
+
+    def h2d():
+        with torch.cuda.stream(up):
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(down):
+            for h, d in zip(host_out, dev_out):
+                h.copy_(d, non_blocking=True)
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    timed(h2d)
+    timed(d2h)
+    t_in, t_out = timed(h2d), timed(d2h)
+    t_both = timed(lambda: (h2d(), d2h()))
+    return {"h2d_gbs": bi / t_in / 1e9, "d2h_gbs": bo / t_out / 1e9, "both_gbs": (bi + bo) / t_both / 1e9,
+            "step_copies_ms": t_both * 1e3, "h2d_bytes": bi, "d2h_bytes": bo, "reps": reps,
+            "how": "best of reps, host clock around a synchronised burst; one cudaMemcpyAsync per tensor"}
+
+
 def time_graph(fn, calls: int, reps: int):
     """Mean device seconds per fn() call: `calls` calls captured in one CUDA
     graph, replayed `reps` times between CUDA events (launches back to back,
@@ -311,13 +379,17 @@ def run_ours(args, world_size, rank, local_rank):
 
     step()
     assert fattn.device_status() == fattn.FA_OK
+    # The sampler covers the contract loop and, right after it, a loop of the
+    # same launches long enough (>= roofline_seconds) for the clock record and
+    # the roofline's mean launch duration to rest on many samples.
     with ClockSampler(gpu_uuid()) as clk:
         total_s, per_launch_s = time_launches(step, args.steps, args.warmup, world_size)
+        roof_per_s, roof_n = time_for(step, args.roofline_seconds, warmup=0)
     clocks = clk.summary()
     assert fattn.device_status() == fattn.FA_OK
     flops = w.flops()
     value = aggregate_throughput(flops, world_size, total_s / args.steps) / 1e12
-    achieved = flops / per_launch_s / 1e12
+    achieved = flops / roof_per_s / 1e12
 
     # ---- end to end through the public API with host buffers: every step
     # copies its Q, K, V in from pinned host memory and its O, LSE back out.
@@ -363,6 +435,11 @@ def run_ours(args, world_size, rank, local_rank):
     e2e_value = aggregate_throughput(flops, world_size, e2e_total / e2e_steps) / 1e12
     h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    # the host link alone, on the same pinned buffers and device tensors
+    link = link_bandwidth([qp, kp, vp], list(dev_in[0]), [op, lp], [o, lse])
+    # an end-to-end step can go no faster than its copies (both directions at
+    # once) or its kernel, whichever is longer
+    e2e_bound = flops / max(link["step_copies_ms"] / 1e3, per_launch_s) / 1e12
     del dev_in, qp, kp, vp
 
     # ---- row softmax workload (second headline): bf16 [4096, 32768] -> bf16 P + fp32 LSE
@@ -370,12 +447,11 @@ def run_ours(args, world_size, rank, local_rank):
     x = inputs.workload_rows_inputs(rw).cuda()
     p = torch.empty_like(x)
     plse = torch.empty(rw.rows, dtype=torch.float32, device="cuda")
-    rsteps = max(20, min(400, args.steps * 2))
-    r_total, r_per = time_launches(lambda: fattn.softmax_rows(x, out=p, lse=plse), rsteps, max(3, args.warmup),
-                                   world_size)
+    r_per, rsteps = time_for(lambda: fattn.softmax_rows(x, out=p, lse=plse), args.extra_seconds,
+                             warmup=max(3, args.warmup))
     r_bytes = rw.rows * rw.cols * 2 * 2 + rw.rows * 4
     r_gbs = r_bytes / r_per / 1e9
-    l_total, l_per = time_launches(lambda: fattn.logsumexp_rows(x, out=plse), rsteps, 3, world_size)
+    l_per, lsteps = time_for(lambda: fattn.logsumexp_rows(x, out=plse), args.extra_seconds)
     l_bytes = rw.rows * rw.cols * 2 + rw.rows * 4
     del x, p
 
@@ -392,6 +468,26 @@ def run_ours(args, world_size, rank, local_rank):
     _, u_per = time_launches(lambda: fattn.attn_fwd(sq, sk, sv, 128 ** -0.5, False, out=so, lse=sl), 20, 3,
                              world_size)
     del sq, sk, sv, ws
+
+    # ---- the other two bf16 attention workloads: d = 64 (inputs 67 MB fit in
+    # L2, so L2 is flushed between launches) and the 32768-key causal one
+    peak_t = peaks["bf16_tflops"]
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    extra_attn = {}
+    for ew, flush in ((inputs.ATTN_B4H16_2048_D64, lambda: flush_buf.zero_()),
+                      (inputs.ATTN_B1H16_32768_D128_CAUSAL, None)):
+        eq, ek, ev = (t.cuda() for t in inputs.workload_attn_inputs(ew))
+        eo = torch.empty_like(eq)
+        el = torch.empty((ew.B, ew.H, ew.N), dtype=torch.float32, device="cuda")
+        e_per, e_n = time_for(lambda: fattn.attn_fwd(eq, ek, ev, ew.scale, ew.causal, out=eo, lse=el),
+                              args.extra_seconds, flush=flush)
+        assert fattn.device_status() == fattn.FA_OK
+        extra_attn[ew.name] = {"value": ew.flops() / e_per / 1e12, "unit": "TFLOP/s", "us_per_launch": e_per * 1e6,
+                               "frac": ew.flops() / e_per / 1e12 / peak_t, "launches": e_n,
+                               "l2": "flushed (256 MB write) between launches" if flush else
+                                     "inputs 403 MB > 129 MB L2, no flush"}
+        del eq, ek, ev, eo, el
+    del flush_buf
 
     # ---- fp32 attention workload (N = M = 64, d = 64): launch-latency bound
     fw = inputs.ATTN_F32_64
@@ -411,7 +507,6 @@ def run_ours(args, world_size, rank, local_rank):
                "sample": f"{nrows} seeded query rows of {w.B * w.H * w.N} ({dt:.1f} s, fp64 three-pass softmax, "
                          f"FLOPs by the same 4*kept*d convention)"}
 
-    peak_t = peaks["bf16_tflops"]
     alg_bytes = (q.numel() + k.numel() + v.numel() + o.numel()) * 2 + lse.numel() * 4
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world_size, "steps": args.steps,
@@ -424,10 +519,14 @@ def run_ours(args, world_size, rank, local_rank):
                      "frac": achieved / peak_t,
                      "traffic": args.traffic if args.traffic is not None else recorded_traffic("attn_bf16_tc"),
                      "algorithmic_bytes": alg_bytes,
-                     "peak_source": f"bf16_tflops (burst), {peak_src}"},
+                     "peak_source": f"bf16_tflops (burst), {peak_src}",
+                     "launches": roof_n, "us_per_launch": roof_per_s * 1e6,
+                     "timed": f"{roof_n} back-to-back launches after the contract loop, one event pair each",
+                     "clocks_samples": clocks.get("samples"), "sm_mhz": clocks.get("sm_mhz")},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipelining": "step i+1's host-to-device copy overlaps step i's kernel and device-to-host copy"},
+                "pipelining": "step i+1's host-to-device copy overlaps step i's kernel and device-to-host copy",
+                "link": link, "bound": e2e_bound, "frac_of_bound": e2e_value / e2e_bound},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "row_softmax": {"workload": rw.name, "value": r_gbs, "unit": "GB/s", "us_per_launch": r_per * 1e6,
@@ -439,7 +538,10 @@ def run_ours(args, world_size, rank, local_rank):
                         "launches": rsteps, "l2": "input 268 MB > 129 MB L2, no flush"},
         "logsumexp_rows": {"workload": rw.name, "value": l_bytes / l_per / 1e9, "unit": "GB/s",
                            "us_per_launch": l_per * 1e6, "frac": l_bytes / l_per / 1e9 / peaks["hbm_gbs"],
-                           "traffic": recorded_traffic("logsumexp_rows_tma"), "bytes_per_launch": l_bytes},
+                           "traffic": recorded_traffic("logsumexp_rows_tma"), "bytes_per_launch": l_bytes,
+                           "launches": lsteps},
+        "attn_b4_h16_n2048_d64": extra_attn[inputs.ATTN_B4H16_2048_D64.name],
+        "attn_b1_h16_n32768_d128_causal": extra_attn[inputs.ATTN_B1H16_32768_D128_CAUSAL.name],
         "attn_splitkv": {"workload": "attn_bf16_B1_H8_N256_M65536_d128 (decode-like)", "splits": nsplit,
                          "value": s_flops / s_per / 1e12, "unit": "TFLOP/s", "us_per_launch": s_per * 1e6,
                          "unsplit_value": s_flops / u_per / 1e12},
@@ -494,6 +596,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--roofline-seconds", type=float, default=1.5,
+                    help="length of the back-to-back loop the roofline's launch duration is taken from")
+    ap.add_argument("--extra-seconds", type=float, default=0.5,
+                    help="seconds of launches for each of the other attention workloads")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per attention launch, if captured for the current kernel")
     ap.add_argument("--rows-traffic", type=float, default=None,

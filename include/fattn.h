@@ -21,8 +21,8 @@
  *    makes the kernel give up, leave its outputs incomplete and record
  *    FA_ERR_DEVICE_TIMEOUT in a per-device status word that
  *    fa_device_status() returns.
- *  - Re-entrant; the only global state is per-device kernel attributes and the
- *    device status word.
+ *  - Re-entrant; the only global state is per-device kernel attributes, the
+ *    device status word and a cache of encoded TMA tensor maps.
  */
 #ifndef FATTN_H
 #define FATTN_H
@@ -65,7 +65,7 @@ typedef enum fa_status {
  *   O    [B, H, N, d]  row-major, dtype out_dtype (written)
  *   LSE  [B, H, N]     fp32, natural log of sum_j exp(scale * q_i . k_j) over
  *                      the keys kept for row i (written; may be NULL = skip)
- *   scale  multiplier of Q K^T (finite, non-zero), usually 1/sqrt(d)
+ *   scale  multiplier of Q K^T: finite and > 0, usually 1/sqrt(d)
  *   causal 0: every key is kept; 1: key j is kept for query i iff j <= i
  *          (top-left aligned, also when N != M); 2: iff j <= i + (M - N)
  *          (bottom-right aligned: the last query sees every key).  A query
@@ -73,9 +73,10 @@ typedef enum fa_status {
  *   in_dtype / out_dtype:
  *      FA_BF16 in  -> tensor-core path, d in {64, 128}; out FA_BF16 or FA_F32
  *      FA_F32  in  -> fp32 CUDA-core path, d in {16, 32, 64, 128}; out FA_F32
- * Errors: FA_ERR_INVALID_ARG for NULL Q/K/V/O, B,H,N,M,d <= 0, a non-finite or
- * zero scale, or sizes whose element count overflows; FA_ERR_UNSUPPORTED for
- * other dtype / d combinations; FA_ERR_MISALIGNED; FA_ERR_CUDA.
+ * Errors: FA_ERR_INVALID_ARG for NULL Q/K/V/O, B,H,N,M,d <= 0, a scale that is
+ * not finite or not > 0, or sizes whose element count overflows;
+ * FA_ERR_UNSUPPORTED for other dtype / d combinations; FA_ERR_MISALIGNED;
+ * FA_ERR_CUDA.
  */
 int fa_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                 int B, int H, int N, int M, int d, float scale, int causal,
@@ -146,8 +147,10 @@ long fa_attn_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits)
  * only its inputs and outputs), or code that must not call cudaMalloc or
  * cudaFree, for instance because cudaFree can synchronise the whole device.
  * Instead of a caller workspace it uses one scratch array of
- * FA_NOALLOC_SCRATCH_BYTES built into the library, which every GPU that loads
- * the library holds until the process exits.  It allocates nothing itself.
+ * FA_NOALLOC_SCRATCH_BYTES built into the library.  A device holds that array
+ * from the moment the library's device code is loaded on it (at the latest the
+ * first call of any libfattn entry point on that device; at once under eager
+ * module loading) until the process exits.  It allocates nothing itself.
  * (The pages have no counterpart: this is a deployment entry point.)
  *
  *   Arguments: as fa_attn_fwd_splitkv, without workspace / workspace_bytes.
@@ -161,6 +164,9 @@ long fa_attn_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits)
  *       call's contents (nothing in it needs to start at zero).  Calls that
  *       overlap on the GPU (other streams, other host threads) race on it;
  *       the caller must serialise them.
+ *   Failures: if a kernel's bounded wait runs out, the combine step may merge
+ *       partials left by an earlier call; O and LSE are defined only when
+ *       fa_device_status() returns FA_OK after the call.
  * Errors: as fa_attn_fwd_splitkv, FA_ERR_INVALID_ARG for the size limit, and
  * FA_ERR_CUDA if the scratch address cannot be looked up.
  */

@@ -6,8 +6,10 @@
 // a plugin only its inputs and outputs), or they must not call cudaMalloc /
 // cudaFree at all, e.g. because cudaFree can synchronise the whole device.
 // fa_attn_fwd_splitkv_noalloc serves them with a fixed scratch array that
-// lives in this library's device image: every GPU that loads the library holds
-// FA_NOALLOC_SCRATCH_BYTES for it until the process exits.
+// lives in this library's device image: a GPU holds FA_NOALLOC_SCRATCH_BYTES
+// for it from the moment the library's device code is loaded there (with lazy
+// module loading, the first libfattn call on that device) until the process
+// exits.
 #include <cstdint>
 #include <mutex>
 
@@ -51,8 +53,10 @@ extern "C" int fa_attn_fwd_splitkv_noalloc(const void* Q, const void* K, const v
                                            int H, int N, int M, int d, float scale, int causal, int num_splits,
                                            int in_dtype, int out_dtype, void* stream) {
     if (B <= 0 || H <= 0 || N <= 0 || M <= 0 || d <= 0) return FA_ERR_INVALID_ARG;
-    if (num_splits < 0 || num_splits > 64) return FA_ERR_INVALID_ARG;
+    if (num_splits < 0) return FA_ERR_INVALID_ARG;
     const int S = num_splits == 0 ? fa_attn_splitkv_num_splits(B, H, N, M, d, causal) : num_splits;
+    // -1 for a split count above the library's maximum (the one limit, kept
+    // where fa_attn_fwd_splitkv checks it)
     const long need = fa_attn_splitkv_workspace_bytes(B, H, N, d, S);
     if (need < 0) return FA_ERR_INVALID_ARG;
     // partials that do not fit the fixed scratch are refused, never truncated

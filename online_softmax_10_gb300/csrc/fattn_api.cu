@@ -1,7 +1,7 @@
 // fattn_api.cu -- the C ABI of libfattn (declared in include/fattn.h).
 //
-// Host side only: argument validation, TMA tensor-map encoding, kernel
-// dispatch on the caller's stream, and the per-device status word that the
+// Host side only: argument validation, TMA tensor-map encoding (with a small
+// cache of recent maps), kernel dispatch on the caller's stream, and the per-device status word that the
 // kernels' bounded waits write on a timeout.
 #include <cmath>
 #include <cstdint>
@@ -89,6 +89,58 @@ bool encode_bf16_4d(CUtensorMap* map, const void* ptr, long B, long H, long rows
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Encoded tensor maps of recent calls.  A map depends only on (pointer,
+// sizes, strides), so a hit is always the map encoding would produce; the
+// cache only saves the driver call (a few microseconds per map, which matters
+// for small problems).  Round-robin replacement, one lock.
+struct MapKey {
+    const void* ptr;
+    long B, H, rows;
+    int d;
+    long long st[3];
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && B == o.B && H == o.H && rows == o.rows && d == o.d && st[0] == o.st[0] &&
+               st[1] == o.st[1] && st[2] == o.st[2];
+    }
+};
+
+class MapCache {
+  public:
+    bool get(const MapKey& k, CUtensorMap* out) {
+        std::lock_guard<std::mutex> lock(mu_);
+        for (int i = 0; i < kSize; ++i)
+            if (used_[i] && keys_[i] == k) {
+                *out = maps_[i];
+                return true;
+            }
+        return false;
+    }
+    void put(const MapKey& k, const CUtensorMap& m) {
+        std::lock_guard<std::mutex> lock(mu_);
+        keys_[next_] = k;
+        maps_[next_] = m;
+        used_[next_] = true;
+        next_ = (next_ + 1) % kSize;
+    }
+
+  private:
+    static constexpr int kSize = 48;
+    std::mutex mu_;
+    MapKey keys_[kSize] = {};
+    CUtensorMap maps_[kSize] = {};
+    bool used_[kSize] = {};
+    int next_ = 0;
+};
+
+bool encode_bf16_4d_cached(CUtensorMap* map, const void* ptr, long B, long H, long rows, int d, const long long* st) {
+    static MapCache cache;
+    const MapKey key{ptr, B, H, rows, d, {st[0], st[1], st[2]}};
+    if (cache.get(key, map)) return true;
+    if (!encode_bf16_4d(map, ptr, B, H, rows, d, st)) return false;
+    cache.put(key, *map);
+    return true;
+}
+
 bool mul_fits(long a, long b, long limit) { return a > 0 && b > 0 && a <= limit / b; }
 
 int num_sms() {
@@ -163,8 +215,8 @@ int attn_launch(const void* Q, const void* K, const void* V, void* O, float* LSE
         e = fa::launch_attn_f32(p, num_sms(), cs);
     } else {
         CUtensorMap tq, tk, tv;
-        if (!encode_bf16_4d(&tq, Q, B, H, N, d, st.q) || !encode_bf16_4d(&tk, K, B, H, M, d, st.k) ||
-            !encode_bf16_4d(&tv, V, B, H, M, d, st.v))
+        if (!encode_bf16_4d_cached(&tq, Q, B, H, N, d, st.q) || !encode_bf16_4d_cached(&tk, K, B, H, M, d, st.k) ||
+            !encode_bf16_4d_cached(&tv, V, B, H, M, d, st.v))
             return FA_ERR_CUDA;
         e = fa::launch_attn_bf16_tc(p, &tq, &tk, &tv, num_sms(), cs);
         if (e == cudaSuccess && S > 1) e = fa::launch_attn_combine(p, cs);

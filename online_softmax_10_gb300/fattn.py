@@ -229,6 +229,8 @@ def attn_fwd_splitkv_noalloc(q, k, v, scale: float | None = None, causal: bool =
     library's fixed 32 MiB scratch instead of a caller workspace.  ``out`` and
     ``lse`` must be given (this call allocates nothing; torch is not asked
     for memory either)."""
+    if out is None or lse is None:
+        raise ValueError("attn_fwd_splitkv_noalloc allocates nothing: pass both out and lse")
     _check_cuda(q, k, v, out, lse)
     B, H, N, d = q.shape
     M = k.shape[2]

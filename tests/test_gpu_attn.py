@@ -1,12 +1,14 @@
 """Parity of fa_attn_fwd (C ABI) with the fp64 oracle.
 
 Tolerances: max-abs 1e-5 on O for fp32 inputs; max-abs 1e-2 on O for bf16
-inputs with fp32 accumulation when O is stored as fp32, plus the bf16 store's
-half-ulp rounding (|O| * 2^-8) when O is stored as bf16; relative 1e-3 on LSE, gated as
+inputs with fp32 accumulation, on O as the kernel computes it (stored as
+fp32); the bf16-stored O must be round-to-nearest-even of that fp32 O bit for
+bit (its own max-abs is reported, not bounded); relative 1e-3 on LSE, gated as
 |dLSE| <= 1e-3 * max(1, |LSE|) because a causal first row's LSE is a single
-score that can be close to zero.
-Full-size workloads are checked on a seeded sample of query rows (each row of
-attention is independent, so a sampled row is an exact check of that row).
+score that can be close to zero.  Every output buffer starts as NaN.
+The two mid-size workloads are checked on every row; the 32768-key workload
+on the first and last row of every 128-row query tile of every head (every
+CTA and both of its tiles) plus a seeded sample.
 """
 import math
 
@@ -15,7 +17,7 @@ import pytest
 import torch
 
 from online_softmax_10_gb300 import fattn, inputs
-from parity import O_TOL_BF16, attn_case, ensure_built
+from parity import O_TOL_BF16, attn_case, default_entry, ensure_built, nan_full, run_attn
 
 pytestmark = pytest.mark.gpu
 
@@ -29,9 +31,7 @@ def _built():
 def test_f32_workload_n64_d64_uniform():
     w = inputs.ATTN_F32_64
     q, k, v = inputs.workload_attn_inputs(w)
-    err, ratio, ok, rel = attn_case(q, k, v, w.causal)
-    assert ratio <= 1.0, err
-    assert ok, rel
+    attn_case(q, k, v, w.causal, name=w.name).assert_ok()
 
 
 @pytest.mark.parametrize("d", [16, 32, 64, 128])
@@ -39,9 +39,7 @@ def test_f32_workload_n64_d64_uniform():
 @pytest.mark.parametrize("N,M", [(1, 1), (63, 65), (130, 70), (70, 130), (200, 200)])
 def test_f32_shapes(d, causal, N, M):
     q, k, v = inputs.attn_inputs(2, 2, N, M, d, torch.float32, seed=N * 7 + M + d)
-    err, ratio, ok, rel = attn_case(q, k, v, causal)
-    assert ratio <= 1.0, err
-    assert ok, rel
+    attn_case(q, k, v, causal).assert_ok()
 
 
 @pytest.mark.parametrize("d", [16, 128])
@@ -50,9 +48,7 @@ def test_f32_many_row_blocks(d, causal):
     """Enough 64-row blocks (32 heads x 10) to fill the GPU twice over: the
     kernel takes 64 rows per CTA instead of 16; ragged last block."""
     q, k, v = inputs.attn_inputs(4, 8, 610, 610, d, torch.float32, seed=610 + d)
-    err, ratio, ok, rel = attn_case(q, k, v, causal)
-    assert ratio <= 1.0, err
-    assert ok, rel
+    attn_case(q, k, v, causal).assert_ok()
 
 
 # ----------------------------------------------------------------- bf16 tensor-core path
@@ -63,20 +59,16 @@ BF16_SHAPES = [(1, 1), (1, 300), (127, 127), (128, 128), (129, 129), (255, 255),
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N,M", BF16_SHAPES)
-@pytest.mark.parametrize("out", ["bf16", "f32"])
-def test_bf16_shapes(d, causal, N, M, out):
+def test_bf16_shapes(d, causal, N, M):
+    # fp32 O against the oracle, bf16 O bit-exact RN of it (attn_case)
     q, k, v = inputs.attn_inputs(1, 2, N, M, d, torch.bfloat16, seed=N + 3 * M + d + causal)
-    err, ratio, ok, rel = attn_case(q, k, v, causal, out_dtype=torch.float32 if out == "f32" else None)
-    assert ratio <= 1.0, err
-    assert ok, rel
+    attn_case(q, k, v, causal).assert_ok()
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_bf16_fp32_output(d):
+def test_bf16_batched_heads_ragged(d):
     q, k, v = inputs.attn_inputs(2, 3, 700, 900, d, torch.bfloat16, seed=d)
-    err, ratio, ok, rel = attn_case(q, k, v, True, out_dtype=torch.float32)
-    assert err <= O_TOL_BF16 and ratio <= 1.0, err
-    assert ok, rel
+    attn_case(q, k, v, True).assert_ok()
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -86,10 +78,7 @@ def test_bf16_many_rescales(d):
     q, k, v = inputs.attn_inputs(1, 2, 384, 1024, d, torch.float32, seed=11)
     ramp = torch.linspace(0.5, 8.0, 1024).reshape(1, 1, 1024, 1)
     k = (k * ramp).to(torch.bfloat16)
-    err, ratio, ok, rel = attn_case(q.to(torch.bfloat16), k, v.to(torch.bfloat16), False,
-                                    out_dtype=torch.float32)
-    assert ratio <= 1.0, err
-    assert ok, rel
+    attn_case(q.to(torch.bfloat16), k, v.to(torch.bfloat16), False).assert_ok()
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -98,7 +87,7 @@ def test_bf16_equal_scores_closed_form(causal):
     N, d = 300, 128
     q, _, v = inputs.attn_inputs(1, 1, N, N, d, torch.bfloat16, seed=4)
     k = torch.zeros_like(q)
-    o, lse = fattn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), 1.0 / math.sqrt(d), causal, out_dtype=torch.float32)
+    o, lse = run_attn(default_entry, q.cuda(), k.cuda(), v.cuda(), 1.0 / math.sqrt(d), causal, torch.float32)
     o, lse = o.cpu().double(), lse.cpu().double()
     vd = v.double()[0, 0]
     if causal:
@@ -113,50 +102,65 @@ def test_bf16_equal_scores_closed_form(causal):
 
 def test_bf16_causal_first_row_is_first_value():
     q, k, v = inputs.attn_inputs(2, 2, 260, 260, 64, torch.bfloat16, seed=9)
-    o, lse = fattn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), 0.125, True)
+    o, lse = run_attn(default_entry, q.cuda(), k.cuda(), v.cuda(), 0.125, True, torch.bfloat16)
     assert torch.equal(o[:, :, 0].cpu(), v[:, :, 0])
 
 
-def _workload_sampled(w, nsample):
-    """The full-size workload in the benchmark's launch configuration (bf16 O),
-    then the same inputs with fp32 O; a seeded sample of rows vs the oracle."""
+def tile_edge_rows(B, H, N, tile=128):
+    """Flat query rows (b*H + h)*N + i: the first and the last row of every
+    `tile`-row query tile of every (batch, head)."""
+    starts = np.arange(0, N, tile)
+    ends = np.minimum(starts + tile, N) - 1
+    per_head = np.unique(np.concatenate([starts, ends]))
+    heads = np.arange(B * H)[:, None] * N
+    return (heads + per_head[None, :]).reshape(-1)
+
+
+def _workload_case(w, rows=None, label="all rows"):
+    """A full-size workload: O as computed within 1e-2 of the oracle, and on
+    these seeded inputs the bf16-stored O (what the benchmark writes) within
+    the same flat 1e-2 as well."""
     q, k, v = inputs.workload_attn_inputs(w)
-    rows = inputs.sample_rows(w.B * w.H * w.N, nsample, seed=w.seed).numpy()
-    for out in (None, torch.float32):
-        err, ratio, ok, rel = attn_case(q, k, v, w.causal, out_dtype=out, rows=rows)
-        assert ratio <= 1.0, (out, err)
-        assert ok, rel
+    res = attn_case(q, k, v, w.causal, rows=rows, name=f"{w.name} ({label})")
+    res.assert_ok()
+    assert res.err_bf16 <= O_TOL_BF16, res.err_bf16
 
 
 def test_bf16_workload_b4_h16_n2048_d64():
-    _workload_sampled(inputs.ATTN_B4H16_2048_D64, 1024)
+    _workload_case(inputs.ATTN_B4H16_2048_D64)
 
 
 def test_bf16_workload_b2_h32_n8192_d128_causal():
-    _workload_sampled(inputs.ATTN_B2H32_8192_D128_CAUSAL, 512)
+    _workload_case(inputs.ATTN_B2H32_8192_D128_CAUSAL)
 
 
 def test_bf16_workload_b1_h16_n32768_d128_causal_kscaled():
-    _workload_sampled(inputs.ATTN_B1H16_32768_D128_CAUSAL, 256)
+    w = inputs.ATTN_B1H16_32768_D128_CAUSAL
+    rows = np.union1d(tile_edge_rows(w.B, w.H, w.N), inputs.sample_rows(w.B * w.H * w.N, 2048, seed=w.seed).numpy())
+    _workload_case(w, rows, f"{len(rows)} rows: both ends of every 128-row tile")
+
+
+def test_tile_edge_rows_cover_every_tile():
+    rows = tile_edge_rows(1, 2, 300)
+    assert list(rows) == [0, 127, 128, 255, 256, 299, 300, 427, 428, 555, 556, 599]
 
 
 def test_bf16_deterministic():
     w = inputs.ATTN_B4H16_2048_D64
     q, k, v = (t.cuda() for t in inputs.workload_attn_inputs(w))
-    o1, l1 = fattn.attn_fwd(q, k, v, w.scale, w.causal)
-    o2, l2 = fattn.attn_fwd(q, k, v, w.scale, w.causal)
-    o3, l3 = fattn.attn_fwd(q, k, v, w.scale, w.causal)
-    assert torch.equal(o1, o2) and torch.equal(o1, o3)
-    assert torch.equal(l1, l2) and torch.equal(l1, l3)
+    outs = [run_attn(default_entry, q, k, v, w.scale, w.causal, torch.bfloat16) for _ in range(3)]
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
 
 
 def test_bf16_side_stream_and_no_lse():
     q, k, v = (t.cuda() for t in inputs.attn_inputs(1, 4, 600, 600, 128, torch.bfloat16, seed=3))
-    ref, _ = fattn.attn_fwd(q, k, v, 0.1, True)
+    ref, _ = run_attn(default_entry, q, k, v, 0.1, True, torch.bfloat16)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
+    o = nan_full(q.shape, torch.bfloat16)
     with torch.cuda.stream(s):
-        o, lse = fattn.attn_fwd(q, k, v, 0.1, True, want_lse=False)
+        o, lse = fattn.attn_fwd(q, k, v, 0.1, True, out=o, want_lse=False)
     s.synchronize()
     assert lse is None
     assert torch.equal(o, ref)
@@ -168,60 +172,55 @@ BR_SHAPES = [(300, 100), (100, 300), (257, 1000), (1000, 257), (1, 300), (300, 1
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N,M", BR_SHAPES)
-@pytest.mark.parametrize("out", ["bf16", "f32"])
-def test_bf16_bottom_right_causal(d, N, M, out):
+def test_bf16_bottom_right_causal(d, N, M):
     # key j kept for query i iff j <= i + (M - N); with N > M the first N - M
     # queries keep no key and must come back as O = 0, LSE = -inf
     q, k, v = inputs.attn_inputs(1, 2, N, M, d, torch.bfloat16, seed=N * 3 + M + d)
-    err, ratio, ok, rel = attn_case(q, k, v, 2, out_dtype=torch.float32 if out == "f32" else None)
-    assert ratio <= 1.0, err
-    assert ok, rel
+    attn_case(q, k, v, 2).assert_ok()
 
 
 @pytest.mark.parametrize("d", [16, 64, 128])
 @pytest.mark.parametrize("N,M", [(70, 130), (130, 70), (1, 40), (40, 1)])
 def test_f32_bottom_right_causal(d, N, M):
     q, k, v = inputs.attn_inputs(2, 2, N, M, d, torch.float32, seed=N + M + d)
-    err, ratio, ok, rel = attn_case(q, k, v, 2)
-    assert ratio <= 1.0, err
-    assert ok, rel
+    attn_case(q, k, v, 2).assert_ok()
 
 
 # ----------------------------------------------------------------- strided layouts
-def _oracle_check(q, k, v, causal, o, lse, o_tol_rel=None):
-    import oracle
-    d = q.shape[-1]
-    O_ref, L_ref = oracle.attn_fwd(q, k, v, 1.0 / math.sqrt(d), causal)
-    og = o.float().cpu().double().numpy()
-    tol = (1e-5 if q.dtype == torch.float32 else 1e-2) + (2.0 ** -8 * np.abs(O_ref) if o.dtype == torch.bfloat16 else 0)
-    assert np.all(np.abs(og - O_ref) <= tol), float(np.max(np.abs(og - O_ref)))
-    from parity import lse_ok
-    ok, rel = lse_ok(lse.cpu().double().numpy(), L_ref)
-    assert ok, rel
-
-
 @pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 64), (torch.bfloat16, 128), (torch.float32, 64)])
 @pytest.mark.parametrize("causal", [0, 1, 2])
 def test_strided_bshd_layout(dtype, d, causal):
     B, H, N, M = 2, 3, 300, 520
     q, k, v = inputs.attn_inputs(B, H, N, M, d, dtype, seed=d + causal)
-    # the same values laid out [B, N, H, d]
-    qs, ks, vs = (t.permute(0, 2, 1, 3).contiguous().cuda() for t in (q, k, v))
-    o, lse = fattn.attn_fwd_strided(qs, ks, vs, causal=causal, layout="bshd")
-    assert fattn.device_status() == fattn.FA_OK
-    assert o.shape == (B, N, H, d)
-    _oracle_check(q, k, v, causal, o.permute(0, 2, 1, 3), lse)
+
+    def entry(q_, k_, v_, scale, causal_, out, lse, stream=None):
+        # the same values laid out [B, N, H, d]; O written [B, N, H, d] in place
+        qs, ks, vs = (t.permute(0, 2, 1, 3).contiguous() for t in (q_, k_, v_))
+        o_bshd = torch.full((B, N, H, d), float("nan"), dtype=out.dtype, device=out.device)
+        o2, _ = fattn.attn_fwd_strided(qs, ks, vs, scale, causal_, out=o_bshd, lse=lse, layout="bshd",
+                                       stream=stream)
+        assert o2.shape == (B, N, H, d)
+        out.copy_(o_bshd.permute(0, 2, 1, 3))
+
+    attn_case(q, k, v, causal, entry=entry).assert_ok()
 
 
 def test_strided_padded_rows_bf16():
     # [B, H, N, d] views cut out of wider rows (row stride 2d) and an output
-    # with a padded row stride as well
+    # with a padded row stride as well; the padding must stay untouched
     B, H, N, M, d = 1, 2, 200, 333, 128
     q, k, v = inputs.attn_inputs(B, H, N, M, d, torch.bfloat16, seed=8)
-    wide = lambda t: torch.cat([t, torch.zeros_like(t)], -1).cuda()[..., :d]
-    qw, kw, vw = wide(q), wide(k), wide(v)
-    ow = torch.zeros(B, H, N, 2 * d, dtype=torch.bfloat16, device="cuda")[..., :d]
-    o, lse = fattn.attn_fwd_strided(qw, kw, vw, causal=1, out=ow, layout="bhsd")
-    assert fattn.device_status() == fattn.FA_OK
-    _oracle_check(q, k, v, 1, o, lse)
-    assert torch.all(ow.as_strided((B, H, N, d), (H * N * 2 * d, N * 2 * d, 2 * d, 1), d) == 0)  # padding untouched
+    pads = []
+
+    def entry(q_, k_, v_, scale, causal_, out, lse, stream=None):
+        wide = lambda t: torch.cat([t, torch.zeros_like(t)], -1)[..., :d]
+        ow_full = torch.zeros(B, H, N, 2 * d, dtype=out.dtype, device=out.device)
+        ow_full[..., :d] = float("nan")
+        ow = ow_full[..., :d]
+        fattn.attn_fwd_strided(wide(q_), wide(k_), wide(v_), scale, causal_, out=ow, lse=lse, layout="bhsd",
+                               stream=stream)
+        pads.append(ow_full[..., d:].clone())
+        out.copy_(ow)
+
+    attn_case(q, k, v, 1, entry=entry).assert_ok()
+    assert all(torch.all(p == 0).item() for p in pads)  # padding untouched
