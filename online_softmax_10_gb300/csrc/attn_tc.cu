@@ -23,11 +23,19 @@
 //   warps 4-7  softmax warpgroup for Q tile 1 (rows q0+128 .. q0+255)
 //   warp  8    TMA producer: Q tiles and K_0 once, then a ring whose slot j
 //              holds V_j and K_{j+1}
-//   warp  9    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+//   warp  9+t  MMA issuer of Q tile t (t = 0, 1): O_t += P_t V_j, then
+//              S_t = Q_t K_{j+1}^T, issued by one elected lane of the warp
+// One issuer per tile: a single issuing thread spends about as long issuing a
+// tile's batch as the tensor core spends running it, so with one issuer for
+// both tiles every batch waited for the other tile's issue as well.
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   S_0 [0,128)  S_1 [128,256)  O_0 [256,256+D)  O_1 [256+D,256+2D)
-// P_t (bf16, two per column) overwrites the first 64 columns of S_t and is the
-// A operand of the P V product straight from tensor memory.
+// P_t (bf16, two per column) is the A operand of the P V product straight
+// from tensor memory.  d = 128: P_t overwrites the first 64 columns of S_t, so
+// the next Q K^T of a tile waits for its P V.  d = 64: the 128 columns left
+// over hold P_0 [384,448) and P_1 [448,512), and the next Q K^T of a tile goes
+// out as soon as its softmax has read S_t into registers; the tile's chain is
+// then its softmax alone.
 // The two softmax warpgroups ping-pong: while one exponentiates, the tensor
 // core runs the other tile's P V and next Q K^T.
 //
@@ -51,9 +59,9 @@ namespace {
 
 constexpr int BM = 128;           // query rows per Q tile
 constexpr int BN = 128;           // keys per K/V tile
-constexpr int kThreads = 320;     // 10 warps
+constexpr int kThreads = 352;     // 11 warps
 constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;       // issuer of Q tile 0; kMmaWarp + 1 issues tile 1
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // base-2 units
 constexpr uint32_t kAtomBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzle atom of a tile
@@ -71,7 +79,9 @@ struct Cfg {
     static constexpr uint32_t kK0 = 2 * kTileBytes;              // K_0
     static constexpr uint32_t kSlot = 3 * kTileBytes;            // slot s: V at +2s tiles, K at +2s+1
     static constexpr uint32_t kBar = kSlot + 2 * NSL * kTileBytes;  // mbarriers
-    static constexpr int kNumBars = 10 + 2 * NSL;
+    // d = 64: P has tensor-memory columns of its own (see the file comment)
+    static constexpr bool kSepP = D == 64;
+    static constexpr int kNumBars = 15 + 3 * NSL;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kSmemBytes = kAbort + 4 + 1024;    // + slack to align the base
@@ -79,17 +89,23 @@ struct Cfg {
     __host__ __device__ static constexpr int QF(int t) { return t; }
     static constexpr int K0F = 2;
     __host__ __device__ static constexpr int FULL(int s) { return 3 + s; }
-    __host__ __device__ static constexpr int EMPTY(int s) { return 3 + NSL + s; }
-    __host__ __device__ static constexpr int SF(int t) { return 3 + 2 * NSL + t; }
-    __host__ __device__ static constexpr int PF(int t) { return 5 + 2 * NSL + t; }
-    __host__ __device__ static constexpr int OD(int t) { return 7 + 2 * NSL + t; }
-    static constexpr int DRAIN = 9 + 2 * NSL;
+    // slot s released by tile t's issuer (each tile releases the fills it used)
+    __host__ __device__ static constexpr int EMPTY(int t, int s) { return 3 + NSL + t * NSL + s; }
+    __host__ __device__ static constexpr int SF(int t) { return 3 + 3 * NSL + t; }
+    __host__ __device__ static constexpr int PF(int t) { return 5 + 3 * NSL + t; }
+    __host__ __device__ static constexpr int OD(int t) { return 7 + 3 * NSL + t; }
+    __host__ __device__ static constexpr int DRAIN(int t) { return 9 + 3 * NSL + t; }
+    // separate-P mode: S_t read into registers (SC), P_t V done (PD)
+    __host__ __device__ static constexpr int SC(int t) { return 11 + 3 * NSL + t; }
+    __host__ __device__ static constexpr int PD(int t) { return 13 + 3 * NSL + t; }
     // tensor-memory columns
     __host__ __device__ static constexpr uint32_t colS(int t) { return (uint32_t)t * 128u; }
     __host__ __device__ static constexpr uint32_t colO(int t) { return 256u + (uint32_t)t * D; }
+    __host__ __device__ static constexpr uint32_t colP(int t) { return kSepP ? 384u + (uint32_t)t * 64u : colS(t); }
 };
 static_assert(Cfg<128>::kSmemBytes <= 227 * 1024, "smem budget (d=128)");
 static_assert(Cfg<64>::kSmemBytes <= 227 * 1024, "smem budget (d=64)");
+static_assert(Cfg<64>::colO(1) + 64 <= Cfg<64>::colP(0) && Cfg<64>::colP(1) + 64 <= 512, "tensor memory (d=64)");
 
 // Number of key tiles Q tile t of the CTA starting at query row q0 must visit.
 // Under the causal mask key j is kept for query i iff j <= i + coff (coff = 0:
@@ -105,55 +121,35 @@ __device__ __forceinline__ int kv_tiles_for(int q0, int t, int N, int M, int cof
     return (int)min((long)nM, last_key / BN + 1);
 }
 
-// Four MMAs into one accumulator (the first accumulates if `acc`), preceded by
-// a non-blocking sample of an mbarrier phase whose result is read only after
-// the fourth MMA: the barrier's round trip to shared memory then overlaps the
-// MMA issue instead of stalling the thread (a predicate cannot outlive one asm
-// block, so both live in the same one).  Returns true if the phase with the
-// given parity had completed when sampled.
-__device__ __forceinline__ bool mma4_ss_sample(uint32_t d_tmem, uint64_t a0, uint64_t a1, uint64_t a2, uint64_t a3,
-                                               uint64_t b0, uint64_t b1, uint64_t b2, uint64_t b3, uint32_t idesc,
-                                               uint32_t acc, uint32_t bar, uint32_t parity) {
-    uint32_t done;
+// One MMA issued by the elected lane of a converged warp: the operands are the
+// same in every lane, so they stay warp-uniform and nothing has to be moved
+// per MMA.  D (+)= A B with A and B from shared-memory descriptors.
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred pt, pa, p1;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 pt, [%12], %13;\n\t"
-        "setp.ne.b32 pa, %11, 0;\n\t"
-        "setp.eq.u32 p1, 0, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %6, %10, pa;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], %3, %7, %10, p1;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], %4, %8, %10, p1;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], %5, %9, %10, p1;\n\t"
-        "selp.u32 %0, 1, 0, pt;\n\t}"
-        : "=r"(done)
-        : "r"(d_tmem), "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
-          "r"(acc), "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
 }
-// The same with A read from tensor memory at a, a + 8, a + 16, a + 24 columns.
-__device__ __forceinline__ bool mma4_ts_sample(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint64_t b1, uint64_t b2,
-                                               uint64_t b3, uint32_t idesc, uint32_t acc, uint32_t bar,
-                                               uint32_t parity) {
-    uint32_t done;
+// The same with A read from tensor memory.
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred pt, pa, p1;\n\t.reg .b32 a1, a2, a3;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 pt, [%9], %10;\n\t"
-        "setp.ne.b32 pa, %8, 0;\n\t"
-        "setp.eq.u32 p1, 0, 0;\n\t"
-        "add.u32 a1, %2, 8;\n\t"
-        "add.u32 a2, %2, 16;\n\t"
-        "add.u32 a3, %2, 24;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %7, pa;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], %4, %7, p1;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], %5, %7, p1;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], %6, %7, p1;\n\t"
-        "selp.u32 %0, 1, 0, pt;\n\t}"
-        : "=r"(done)
-        : "r"(d_tmem), "r"(a_tmem), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc), "r"(acc), "r"(bar),
-          "r"(parity)
-        : "memory");
-    return done != 0;
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
+}
+// Arrive once on `bar` when every MMA the elected lane issued so far has completed.
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        :: "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void record_failure(volatile int* abort_flag, int* status) {
@@ -206,7 +202,8 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == C::PF(0) || i == C::PF(1)) count = BM;  // one arrival per softmax thread
+            if (i == C::PF(0) || i == C::PF(1) || i == C::SC(0) || i == C::SC(1))
+                count = BM;  // one arrival per softmax thread
             mbar_init(bar(i), count);
         }
         *abort_flag = 0;
@@ -246,7 +243,13 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             for (int c = 0; c < nk; ++c) {
                 const int sl = c % C::NSL;
                 const uint32_t ph = (uint32_t)(c / C::NSL) & 1u;
-                if (!mbar_wait_bounded(bar(C::EMPTY(sl)), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                // the slot's previous fill (c - NSL) is free once every tile
+                // that used it has released it
+                bool free_ok = true;
+                for (int t = 0; t < 2 && free_ok; ++t)
+                    if (c >= C::NSL && c - C::NSL < (t == 0 ? n0 : n1))
+                        free_ok = mbar_wait_bounded(bar(C::EMPTY(t, sl)), ph ^ 1u, abort_flag, kWaitLimitNs);
+                if (!free_ok) {
                     record_failure(abort_flag, status);
                     break;
                 }
@@ -270,122 +273,97 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             for (int t = 0; t < 2; ++t)
                 if ((t == 0 ? n0 : n1) > 0) mbar_wait_bounded(bar(C::QF(t)), 0, nullptr, kWaitLimitNs);
         }
-    } else if (warp == kMmaWarp) {
-        // -------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
-            constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);    // P from TMEM, V MN-major
-            const int nt[2] = {n0, n1};
-            // Issuing one tcgen05.mma takes this thread about as long as the
-            // tensor pipe needs to run a 128x128x16 one, so every instruction
-            // it spends between MMAs shows up as pipe idle time.  Descriptors
-            // are therefore built once: the start-address field (address / 16,
-            // 14 bits) of every operand block follows by adding its offset / 16
-            // (shared addresses stay below 256 KB, so the field cannot carry).
-            const uint64_t dQ = umma_desc_sw128(base + C::kQ, 16, 1024);
-            const uint64_t dK0 = umma_desc_sw128(base + C::kK0, 16, 1024);
-            const uint64_t dK = umma_desc_sw128(base + C::kSlot + C::kTileBytes, 16, 1024);
-            const uint64_t dV = umma_desc_sw128(base + C::kSlot, kAtomBytes, 1024);
-            constexpr uint32_t kSlotStep = 2 * C::kTileBytes >> 4;
-            // kb: descriptor of the K tile (K_0's buffer or a slot's K half)
-            auto issue_S = [&](int t, uint64_t kb) {
-                const uint64_t qa = dQ + ((uint32_t)t * C::kTileBytes >> 4);
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // -------------------------------------------------------- MMA issuer of tile t
+        // The whole warp runs this code with the same values in every lane;
+        // one elected lane issues each MMA and commit.
+        const int t = warp - kMmaWarp;
+        const int n = t == 0 ? n0 : n1;
+        constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
+        constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);    // P from TMEM, V MN-major
+        // Descriptors are built once: the start-address field (address / 16,
+        // 14 bits) of every operand block follows by adding its offset / 16
+        // (shared addresses stay below 256 KB, so the field cannot carry).
+        const uint64_t dQ = umma_desc_sw128(base + C::kQ + (uint32_t)t * C::kTileBytes, 16, 1024);
+        const uint64_t dK0 = umma_desc_sw128(base + C::kK0, 16, 1024);
+        const uint64_t dK = umma_desc_sw128(base + C::kSlot + C::kTileBytes, 16, 1024);
+        const uint64_t dV = umma_desc_sw128(base + C::kSlot, kAtomBytes, 1024);
+        constexpr uint32_t kSlotStep = 2 * C::kTileBytes >> 4;
+        const uint32_t tS = tmem + C::colS(t);
+        const uint32_t tO = tmem + C::colO(t);
+        const uint32_t tP = tmem + C::colP(t);
+        // S_t = Q_t K^T, K at descriptor kb (K_0's buffer or a slot's K half)
+        auto issue_S = [&](uint64_t kb) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((uint32_t)(kk >> 2) * kAtomBytes + (uint32_t)(kk & 3) * 32u) >> 4;
-                    mma_ss(tmem + C::colS(t), qa + off, kb + off, idS, kk > 0 ? 1u : 0u);
-                }
-            };
-            bool ok = true;
-            for (int t = 0; t < 2 && ok; ++t)
-                if (nt[t] > 0) ok = mbar_wait_bounded(bar(C::QF(t)), 0, abort_flag, kWaitLimitNs);
-            // (a split may hold no key tile at all: then nothing is issued)
-            if (ok && nk > 0) ok = mbar_wait_bounded(bar(C::K0F), 0, abort_flag, kWaitLimitNs);
-            if (ok && nk > 0) {
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((uint32_t)(kk >> 2) * kAtomBytes + (uint32_t)(kk & 3) * 32u) >> 4;
+                mma_ss_elect(tS, dQ + off, kb + off, idS, kk > 0 ? 1u : 0u);
+            }
+        };
+        // O_t (+)= P_t V, V in ring slot sl, P_t (bf16, 64 columns) at tP
+        auto issue_PV = [&](int sl, uint32_t acc_first) {
+            const uint64_t vb = dV + (uint32_t)sl * kSlotStep;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+                mma_ts_elect(tO, tP + (uint32_t)kk * 8u, vb + (uint32_t)kk * 128u, idO, kk > 0 ? 1u : acc_first);
+        };
+        auto wait_all = [&](int b, uint32_t parity) -> bool {
+            return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(b), parity, abort_flag, kWaitLimitNs));
+        };
+        bool ok = true;
+        if (n > 0) {
+            ok = wait_all(C::QF(t), 0) && wait_all(C::K0F, 0);
+            // tile 1 starts once tile 0's first scores are done, so the two
+            // tiles' softmaxes begin half a step apart and alternate from there
+            if (ok && t == 1 && n0 > 0) ok = wait_all(C::SF(0), 0);
+            if (ok) {
                 tc_fence_after();
-                for (int t = 0; t < 2; ++t) {
-                    if (nt[t] == 0) continue;
-                    issue_S(t, dK0);
-                    mma_commit(bar(C::SF(t)));
-                }
+                issue_S(dK0);
+                mma_commit_elect(bar(C::SF(t)));
             }
-            // MMAs go out in groups of four, each also sampling an mbarrier whose
-            // answer is read only after the group: tile 0's last group samples
-            // P_1 of this step, tile 1's first group the next step's K/V slot
-            // and its last group P_0 of the next step.  A barrier found
-            // complete is not waited for again; the sample's round trip hides
-            // behind the MMA issue (each wait would otherwise idle the pipe).
-            auto pv_quad = [&](int t, int sl, int q, uint32_t acc, uint32_t sbar, uint32_t spar) -> bool {
-                const uint64_t vb = dV + (uint32_t)sl * kSlotStep + (uint32_t)q * 512u;
-                return mma4_ts_sample(tmem + C::colO(t), tmem + C::colS(t) + (uint32_t)q * 32u, vb, vb + 128u,
-                                      vb + 256u, vb + 384u, idO, acc, sbar, spar);
-            };
-            auto s_quad = [&](int t, uint64_t kb, int q, uint32_t sbar, uint32_t spar) -> bool {
-                const uint64_t qa = dQ + ((uint32_t)t * C::kTileBytes >> 4) + (uint32_t)q * (kAtomBytes >> 4);
-                const uint64_t kq = kb + (uint32_t)q * (kAtomBytes >> 4);
-                return mma4_ss_sample(tmem + C::colS(t), qa, qa + 2u, qa + 4u, qa + 6u, kq, kq + 2u, kq + 4u, kq + 6u,
-                                      idS, q > 0 ? 1u : 0u, sbar, spar);
-            };
-            constexpr int kSQuads = D / 64;
-            bool full_ok = false, pf0_ok = false;
-            for (int j = 0; j < nk && ok; ++j) {
-                const int sl = j % C::NSL;
-                const uint32_t ph = (uint32_t)(j / C::NSL) & 1u;
-                const uint32_t pj = (uint32_t)j & 1u;
-                const int jn = j + 1;
-                // V_j and K_{j+1}, then per Q tile P_j V_j and Q K_{j+1}^T back to back
-                if (!full_ok && !(ok = mbar_wait_bounded(bar(C::FULL(sl)), ph, abort_flag, kWaitLimitNs))) break;
-                full_ok = false;
-                bool pf1_ok = false, pf0_next = false;
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (!ok || j >= nt[t]) continue;
-                    const bool ready = t == 0 ? pf0_ok : pf1_ok;
-                    if (!ready && !(ok = mbar_wait_bounded(bar(C::PF(t)), pj, abort_flag, kWaitLimitNs))) break;
-                    tc_fence_after();
-                    // sample targets; QF(t) (long complete) where there is nothing to sample
-                    const uint32_t dummy = bar(C::QF(t));
-                    uint32_t fb = dummy, fp = 0, lb = dummy, lp = 0;
-                    if (t == 1 && jn < nk) {
-                        fb = bar(C::FULL(jn % C::NSL));
-                        fp = (uint32_t)(jn / C::NSL) & 1u;
-                    }
-                    if (t == 0 && j < nt[1]) {
-                        lb = bar(C::PF(1));
-                        lp = pj;
-                    }
-                    if (t == 1 && jn < nt[0]) {
-                        lb = bar(C::PF(0));
-                        lp = pj ^ 1u;
-                    }
-                    const bool has_next = jn < nt[t];
-                    const bool f_res = pv_quad(t, sl, 0, j > 0 ? 1u : 0u, fb, fp);
-                    bool l_res;
-                    if (!has_next) {
-                        l_res = pv_quad(t, sl, 1, 1u, lb, lp);
-                        if (j == nt[t] - 1) mma_commit(bar(C::OD(t)));
-                    } else {
-                        pv_quad(t, sl, 1, 1u, dummy, 0);
-                        const uint64_t kb = dK + (uint32_t)sl * kSlotStep;
-#pragma unroll
-                        for (int q = 0; q + 1 < kSQuads; ++q) s_quad(t, kb, q, dummy, 0);
-                        l_res = s_quad(t, kb, kSQuads - 1, lb, lp);
-                        mma_commit(bar(C::SF(t)));
-                    }
-                    if (t == 0) pf1_ok = l_res && lb != dummy;
-                    if (t == 1) {
-                        full_ok = f_res && fb != dummy;
-                        pf0_next = l_res && lb != dummy;
-                    }
-                }
-                mma_commit(bar(C::EMPTY(sl)));
-                pf0_ok = pf0_next;
-            }
-            if (!ok) record_failure(abort_flag, status);
-            // Drain: every MMA issued above has completed before TMEM is freed.
-            mma_commit(bar(C::DRAIN));
-            mbar_wait_bounded(bar(C::DRAIN), 0, nullptr, kWaitLimitNs);
         }
+        // key step j: wait for V_j / K_{j+1} and for this tile's P_j, then
+        // P_j V_j and (unless this was the tile's last step) Q K_{j+1}^T back
+        // to back; the P V MMAs read P_j before Q K_{j+1}^T overwrites it
+        // because one thread issues both, in order
+        for (int j = 0; j < n && ok; ++j) {
+            const int sl = j % C::NSL;
+            const uint32_t ph = (uint32_t)(j / C::NSL) & 1u;
+            const uint32_t pj = (uint32_t)j & 1u;
+            if constexpr (C::kSepP) {
+                // Q K_{j+1}^T as soon as the softmax has read S_j, then P_j V_j
+                ok = wait_all(C::FULL(sl), ph);
+                if (ok && j + 1 < n) {
+                    ok = wait_all(C::SC(t), pj);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_S(dK + (uint32_t)sl * kSlotStep);
+                    mma_commit_elect(bar(C::SF(t)));
+                }
+                ok = ok && wait_all(C::PF(t), pj);
+                if (!ok) break;
+                tc_fence_after();
+                issue_PV(sl, j > 0 ? 1u : 0u);
+                mma_commit_elect(bar(C::PD(t)));
+                if (j + 1 == n) mma_commit_elect(bar(C::OD(t)));
+            } else {
+                ok = wait_all(C::FULL(sl), ph) && wait_all(C::PF(t), pj);
+                if (!ok) break;
+                tc_fence_after();
+                issue_PV(sl, j > 0 ? 1u : 0u);
+                if (j + 1 < n) {
+                    issue_S(dK + (uint32_t)sl * kSlotStep);
+                    mma_commit_elect(bar(C::SF(t)));
+                } else {
+                    mma_commit_elect(bar(C::OD(t)));
+                }
+            }
+            mma_commit_elect(bar(C::EMPTY(t, sl)));
+        }
+        if (!ok && lane == 0) record_failure(abort_flag, status);
+        // Drain: every MMA issued above has completed before TMEM is freed.
+        mma_commit_elect(bar(C::DRAIN(t)));
+        mbar_wait_bounded(bar(C::DRAIN(t)), 0, nullptr, kWaitLimitNs);
         __syncwarp();
     } else {
         // -------------------------------------------------------- softmax warpgroups
@@ -396,6 +374,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
         const uint32_t tS = tl + C::colS(t);
         const uint32_t tO = tl + C::colO(t);
+        const uint32_t tP = tl + C::colP(t);
         const int n = t == 0 ? n0 : n1;
         float m = -CUDART_INF_F;  // running max (base-2 units), possibly stale by < 8
         float l = 0.f;            // running sum of p relative to m
@@ -407,6 +386,11 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             tc_fence_after();
             uint32_t sr[128];
             tmem_ld_x128(tS, sr);
+            if constexpr (C::kSepP) {
+                // S_t is in registers: the tile's next Q K^T may overwrite it
+                tc_fence_before();
+                mbar_arrive(bar(C::SC(t)));
+            }
             float sv[128];
 #pragma unroll
             for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
@@ -442,7 +426,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
             }
             // p = 2^(s * scale * log2e - m), two lanes per packed FMA; P (bf16)
-            // overwrites S in tensor memory
+            // goes to tensor memory (over S_t, or its own columns for d = 64)
             const float neg_m = m == -CUDART_INF_F ? 0.f : -m;
             const float2 cc = make_float2(c_log2, c_log2), nm = make_float2(neg_m, neg_m);
             float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -457,10 +441,20 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
             const float2 lsum = add2(add2(ls[0], ls[1]), add2(ls[2], ls[3]));
             l = fmaf(l, alpha, lsum.x + lsum.y);
-            tmem_st_x64(tS, pk);
+            if constexpr (C::kSepP) {
+                // P_t and O_t are free once the previous P V of this tile is done
+                if (j > 0) {
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(C::PD(t)), (uint32_t)(j - 1) & 1u, abort_flag,
+                                                                   kWaitLimitNs));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+            }
+            tmem_st_x64(tP, pk);
             // o~ <- alpha o~ when the reference max was raised.  The previous
-            // P V of this tile has completed: it was issued before the Q K^T
-            // whose completion this warpgroup just waited for.
+            // P V of this tile has completed: with P over S it was issued
+            // before the Q K^T whose completion this warpgroup waited for, with
+            // P apart the PD wait above saw it done.
             if (__any_sync(0xFFFFFFFFu, rescale)) {
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
