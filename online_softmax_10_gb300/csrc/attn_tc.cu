@@ -163,7 +163,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     const __grid_constant__ CUtensorMap tmV, void* __restrict__ O, float* __restrict__ LSE,
                     int N, int M, float c_log2, int out_bf16, int* status, int nqb, int BH, int G, int S,
                     float* __restrict__ Opart, float* __restrict__ Lpart, int H, int coff, long long osb,
-                    long long osh, long long osr) {
+                    long long osh, long long osr, int npair) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -176,21 +176,26 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // unit -> (head, query block, key split): groups of G heads, longest block
-    // first, the S splits of a block adjacent
-    const int split = (int)(blockIdx.x % (unsigned)S);
-    const int u = (int)(blockIdx.x / (unsigned)S);
+    // first, the S splits of a block adjacent.  CTAs from npair on (S = 1
+    // only) take one 128-row half of a unit each ("single" CTAs): the launch
+    // uses them for a last wave that would otherwise leave most SMs idle.
+    const bool single = (int)blockIdx.x >= npair;
+    const int split = single ? 0 : (int)(blockIdx.x % (unsigned)S);
+    const int u = single ? npair + ((int)blockIdx.x - npair) / 2 : (int)(blockIdx.x / (unsigned)S);
+    const int half = single ? ((int)blockIdx.x - npair) & 1 : 0;
     const int g0 = (u / (G * nqb)) * G;
     const int gh = min(G, BH - g0);
     const int r = u - g0 * nqb;
     const long bh = g0 + r % gh;
     const int qblk = nqb - 1 - r / gh;
-    const int q0 = qblk * 2 * BM;
+    const int q0 = qblk * 2 * BM + half * BM;
     const int hh = (int)(bh % H), bb = (int)(bh / H);  // head, batch (tensor-map coordinates)
     // This CTA covers key tiles [jb, jb + nk) of the ones its query block
     // needs (all of them when S = 1); n0, n1 count the tiles of that range each
-    // Q tile uses, and j below runs over the range (key tile jb + j).
+    // Q tile uses, and j below runs over the range (key tile jb + j).  A single
+    // CTA has no tile 1.
     const int f0 = kv_tiles_for<CAUSAL>(q0, 0, N, M, coff);
-    const int f1 = kv_tiles_for<CAUSAL>(q0, 1, N, M, coff);
+    const int f1 = single ? 0 : kv_tiles_for<CAUSAL>(q0, 1, N, M, coff);
     const int fk = max(f0, f1);
     const int jb = (int)((long)split * fk / S);
     const int je = (int)((long)(split + 1) * fk / S);
@@ -199,7 +204,10 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int nk = je - jb;
 
     // ------------------------------------------------------------ set-up
-    if (threadIdx.x == 0) {
+    // The producer lane initialises every barrier and issues the Q and K_0
+    // copies before the CTA-wide barrier, so those loads overlap the tensor-
+    // memory allocation and the first synchronisation.
+    if (warp == kLoadWarp && lane == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
             if (i == C::PF(0) || i == C::PF(1) || i == C::SC(0) || i == C::SC(1))
@@ -208,11 +216,22 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
         *abort_flag = 0;
         fence_mbar_init();
-    }
-    if (warp == kLoadWarp && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        const uint64_t pol_q = l2_policy_evict_first();
+        for (int t = 0; t < 2; ++t) {
+            if ((t == 0 ? n0 : n1) == 0) continue;
+            mbar_expect_tx(bar(C::QF(t)), C::kTileBytes);
+            for (int a = 0; a < C::kAtoms; ++a)
+                tma_load_4d_hint(base + C::kQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar(C::QF(t)), a * 64,
+                                 q0 + t * BM, hh, bb, pol_q);
+        }
+        if (nk > 0) {
+            mbar_expect_tx(bar(C::K0F), C::kTileBytes);
+            for (int a = 0; a < C::kAtoms; ++a)
+                tma_load_4d(base + C::kK0 + a * kAtomBytes, &tmK, bar(C::K0F), a * 64, jb * BN, hh, bb);
+        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(base + C::kTmemSlot, kTmemCols);
@@ -225,20 +244,8 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
     if (warp == kLoadWarp) {
         // -------------------------------------------------------- TMA producer
+        // (Q and K_0 are already in flight, issued during set-up.)
         if (lane == 0) {
-            const uint64_t pol_q = l2_policy_evict_first();
-            for (int t = 0; t < 2; ++t) {
-                if ((t == 0 ? n0 : n1) == 0) continue;
-                mbar_expect_tx(bar(C::QF(t)), C::kTileBytes);
-                for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_4d_hint(base + C::kQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar(C::QF(t)),
-                                     a * 64, q0 + t * BM, hh, bb, pol_q);
-            }
-            if (nk > 0) {
-                mbar_expect_tx(bar(C::K0F), C::kTileBytes);
-                for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_4d(base + C::kK0 + a * kAtomBytes, &tmK, bar(C::K0F), a * 64, jb * BN, hh, bb);
-            }
             int issued = 0;
             for (int c = 0; c < nk; ++c) {
                 const int sl = c % C::NSL;
@@ -379,17 +386,22 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         float m = -CUDART_INF_F;  // running max (base-2 units), possibly stale by < 8
         float l = 0.f;            // running sum of p relative to m
         bool ok = true;
+        bool s_ready = false;     // S_j already seen complete by an early probe
         for (int j = 0; j < n; ++j) {
-            ok = mbar_wait_bounded(bar(C::SF(t)), (uint32_t)j & 1u, abort_flag, kWaitLimitNs);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (!ok) break;
+            if (!__all_sync(0xFFFFFFFFu, s_ready)) {
+                ok = mbar_wait_bounded(bar(C::SF(t)), (uint32_t)j & 1u, abort_flag, kWaitLimitNs);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+            }
             tc_fence_after();
             uint32_t sr[128];
             tmem_ld_x128(tS, sr);
+            bool pd_ready = true;  // the previous P V of this tile is done (separate-P mode)
             if constexpr (C::kSepP) {
                 // S_t is in registers: the tile's next Q K^T may overwrite it
                 tc_fence_before();
                 mbar_arrive(bar(C::SC(t)));
+                if (j > 0) pd_ready = mbar_test(bar(C::PD(t)), (uint32_t)(j - 1) & 1u);
             }
             float sv[128];
 #pragma unroll
@@ -403,16 +415,16 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     if (key >= M || (CAUSAL && key > qi + coff)) sv[c] = -CUDART_INF_F;
                 }
             }
-            // row max: three-input max over four independent chains
-            float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+            // row max: three-input max over eight independent chains
+            float mx[8];
 #pragma unroll
-            for (int c = 0; c < 128; c += 8) {
-                mx[0] = max3f(mx[0], sv[c], sv[c + 1]);
-                mx[1] = max3f(mx[1], sv[c + 2], sv[c + 3]);
-                mx[2] = max3f(mx[2], sv[c + 4], sv[c + 5]);
-                mx[3] = max3f(mx[3], sv[c + 6], sv[c + 7]);
-            }
-            const float m_tile = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c_log2;
+            for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[2 * i], sv[2 * i + 1]);
+#pragma unroll
+            for (int c = 16; c < 128; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = max3f(mx[i], sv[c + 2 * i], sv[c + 2 * i + 1]);
+            const float m_tile =
+                max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c_log2;
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -441,12 +453,16 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
             const float2 lsum = add2(add2(ls[0], ls[1]), add2(ls[2], ls[3]));
             l = fmaf(l, alpha, lsum.x + lsum.y);
+            // probe for the next scores now; read at the top of the next step
+            s_ready = j + 1 < n && mbar_test(bar(C::SF(t)), (uint32_t)(j + 1) & 1u);
             if constexpr (C::kSepP) {
                 // P_t and O_t are free once the previous P V of this tile is done
                 if (j > 0) {
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(C::PD(t)), (uint32_t)(j - 1) & 1u, abort_flag,
-                                                                   kWaitLimitNs));
-                    if (!ok) break;
+                    if (!__all_sync(0xFFFFFFFFu, pd_ready)) {
+                        ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(C::PD(t)), (uint32_t)(j - 1) & 1u,
+                                                                       abort_flag, kWaitLimitNs));
+                        if (!ok) break;
+                    }
                     tc_fence_after();
                 }
             }
@@ -472,7 +488,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // ------------------------------------------------------ epilogue
         const long orow = bh * (long)N + qi;                       // LSE / partial index
         const long obase = bb * osb + hh * osh + (long)qi * osr;   // O element offset (strided)
-        const bool store = qi < N;
+        const bool store = qi < N && !(single && t == 1);
         if (n == 0 && ok && store) {
             // no key of this range is kept for this row
             if (S > 1) {
@@ -574,12 +590,24 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtenso
     int G = (2 * num_sms + nqb - 1) / nqb;
     G = G < 1 ? 1 : (G > BH ? BH : G);
     const int S = p.num_splits > 1 ? p.num_splits : 1;
-    const dim3 grid((unsigned)((long)nqb * BH * S));
+    const long units = (long)nqb * BH;
+    long npair = units * S, ncta = npair;
+    // Without the causal mask every unit takes the same time, so a last wave
+    // of k < SMs/2 units would leave most SMs idle: those k units run as 2k
+    // single-tile CTAs instead, each about 0.6 of a unit's time.
+    if (S == 1 && !CAUSAL) {
+        const long k = units % num_sms;
+        if (units >= num_sms && k > 0 && 2 * k <= num_sms) {
+            npair = units - k;
+            ncta = npair + 2 * k;
+        }
+    }
+    const dim3 grid((unsigned)ncta);
     const float c_log2 = p.scale * 1.4426950408889634f;
     const int coff = p.causal == 2 ? p.M - p.N : 0;
     kern<<<grid, kThreads, Cf::kSmemBytes, st>>>(*tmQ, *tmK, *tmV, p.O, p.LSE, p.N, p.M, c_log2, p.out_bf16, p.status,
                                                  nqb, BH, G, S, p.Opart, p.Lpart, p.H, coff, p.os[0], p.os[1],
-                                                 p.os[2]);
+                                                 p.os[2], (int)npair);
     return cudaGetLastError();
 }
 

@@ -72,6 +72,18 @@ def test_bf16_batched_heads_ragged(d):
 
 
 @pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [300, 512])
+def test_bf16_last_wave_single_tile_ctas(d, N):
+    """Without the causal mask, a last wave of k <= SMs/2 (head, 256-row block)
+    units runs as 2k CTAs of one 128-row tile each.  SMs + 8 units put 8 units
+    there; with N = 300 some of those halves hold 44 rows or none."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = (sms + 8) // 2
+    q, k, v = inputs.attn_inputs(1, H, N, 500, d, torch.bfloat16, seed=N + d)
+    attn_case(q, k, v, False).assert_ok()
+
+
+@pytest.mark.parametrize("d", [64, 128])
 def test_bf16_many_rescales(d):
     # K scaled x8 and sorted-growing score scale along the keys: the running
     # max rises repeatedly, exercising the conditional rescale of o~.
