@@ -59,25 +59,30 @@ namespace {
 
 constexpr int BM = 128;           // query rows per Q tile
 constexpr int BN = 128;           // keys per K/V tile
-constexpr int kThreads = 352;     // 11 warps
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;       // issuer of Q tile 0; kMmaWarp + 1 issues tile 1
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // base-2 units
 constexpr uint32_t kAtomBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzle atom of a tile
-constexpr uint32_t kTmemCols = 512;
 
-template <int D>
+// D: head dimension; NT: Q tiles (of 128 rows) per CTA.  NT = 2 runs one CTA
+// per SM whose two tiles share every K/V tile; NT = 1 (d = 64) runs two CTAs
+// per SM, each with a quarter of the tensor memory and under half the shared
+// memory, so one CTA's set-up and epilogue overlap the other's key steps.
+template <int D, int NT>
 struct Cfg {
+    static constexpr int kThreads = 32 * (5 * NT + 1);           // 4 softmax warps + 1 issuer per tile, 1 producer
+    static constexpr int kLoadWarp = 4 * NT;
+    static constexpr int kMmaWarp = 4 * NT + 1;                  // issuer of tile t: kMmaWarp + t
+    static constexpr int kMinBlocks = NT == 1 ? 2 : 1;           // CTAs resident per SM
+    static constexpr uint32_t kTmemCols = NT == 2 ? 512 : 256;
     static constexpr int kAtoms = D / 64;                        // 128-byte column blocks per row
     static constexpr uint32_t kTileBytes = (uint32_t)BM * D * 2; // one 128-row bf16 tile
     // Key/value ring: slot j holds V_j and K_{j+1}, the two tiles key step j
     // of the MMA issuer reads (P_j V_j, then Q K_{j+1}^T), so one full and one
     // empty barrier per step cover both.  K_0 has a buffer of its own.
-    static constexpr int NSL = D == 128 ? 2 : 4;                 // ring slots
-    static constexpr uint32_t kQ = 0;                            // Q_0, Q_1
-    static constexpr uint32_t kK0 = 2 * kTileBytes;              // K_0
-    static constexpr uint32_t kSlot = 3 * kTileBytes;            // slot s: V at +2s tiles, K at +2s+1
+    static constexpr int NSL = (D == 64 && NT == 2) ? 4 : 2;     // ring slots
+    static constexpr uint32_t kQ = 0;                            // Q_0 .. Q_{NT-1}
+    static constexpr uint32_t kK0 = NT * kTileBytes;             // K_0
+    static constexpr uint32_t kSlot = (NT + 1) * kTileBytes;     // slot s: V at +2s tiles, K at +2s+1
     static constexpr uint32_t kBar = kSlot + 2 * NSL * kTileBytes;  // mbarriers
     // d = 64: P has tensor-memory columns of its own (see the file comment)
     static constexpr bool kSepP = D == 64;
@@ -98,14 +103,17 @@ struct Cfg {
     // separate-P mode: S_t read into registers (SC), P_t V done (PD)
     __host__ __device__ static constexpr int SC(int t) { return 11 + 3 * NSL + t; }
     __host__ __device__ static constexpr int PD(int t) { return 13 + 3 * NSL + t; }
-    // tensor-memory columns
+    // tensor-memory columns: S_t, then O_t, then (d = 64) P_t
     __host__ __device__ static constexpr uint32_t colS(int t) { return (uint32_t)t * 128u; }
-    __host__ __device__ static constexpr uint32_t colO(int t) { return 256u + (uint32_t)t * D; }
-    __host__ __device__ static constexpr uint32_t colP(int t) { return kSepP ? 384u + (uint32_t)t * 64u : colS(t); }
+    __host__ __device__ static constexpr uint32_t colO(int t) { return NT * 128u + (uint32_t)t * D; }
+    __host__ __device__ static constexpr uint32_t colP(int t) {
+        return kSepP ? NT * (128u + D) + (uint32_t)t * 64u : colS(t);
+    }
 };
-static_assert(Cfg<128>::kSmemBytes <= 227 * 1024, "smem budget (d=128)");
-static_assert(Cfg<64>::kSmemBytes <= 227 * 1024, "smem budget (d=64)");
-static_assert(Cfg<64>::colO(1) + 64 <= Cfg<64>::colP(0) && Cfg<64>::colP(1) + 64 <= 512, "tensor memory (d=64)");
+static_assert(Cfg<128, 2>::kSmemBytes <= 227 * 1024, "smem budget (d=128)");
+static_assert(2 * (Cfg<64, 1>::kSmemBytes + 1024) <= 228 * 1024, "smem budget (d=64, two CTAs per SM)");
+static_assert(Cfg<64, 1>::colP(0) + 64 <= Cfg<64, 1>::kTmemCols, "tensor memory (d=64)");
+static_assert(Cfg<128, 2>::colO(1) + 128 <= Cfg<128, 2>::kTmemCols, "tensor memory (d=128)");
 
 // Number of key tiles Q tile t of the CTA starting at query row q0 must visit.
 // Under the causal mask key j is kept for query i iff j <= i + coff (coff = 0:
@@ -157,14 +165,16 @@ __device__ __forceinline__ void record_failure(volatile int* abort_flag, int* st
     atomicExch(status, kDevStatusTimeout);
 }
 
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool CAUSAL, int NT>
+__global__ void __launch_bounds__(Cfg<D, NT>::kThreads, Cfg<D, NT>::kMinBlocks)
 attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, void* __restrict__ O, float* __restrict__ LSE,
                     int N, int M, float c_log2, int out_bf16, int* status, int nqb, int BH, int G, int S,
                     float* __restrict__ Opart, float* __restrict__ Lpart, int H, int coff, long long osb,
                     long long osh, long long osr, int npair) {
-    using C = Cfg<D>;
+    using C = Cfg<D, NT>;
+    constexpr int kLoadWarp = C::kLoadWarp;
+    constexpr int kMmaWarp = C::kMmaWarp;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -179,16 +189,17 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // first, the S splits of a block adjacent.  CTAs from npair on (S = 1
     // only) take one 128-row half of a unit each ("single" CTAs): the launch
     // uses them for a last wave that would otherwise leave most SMs idle.
-    const bool single = (int)blockIdx.x >= npair;
-    const int split = single ? 0 : (int)(blockIdx.x % (unsigned)S);
-    const int u = single ? npair + ((int)blockIdx.x - npair) / 2 : (int)(blockIdx.x / (unsigned)S);
-    const int half = single ? ((int)blockIdx.x - npair) & 1 : 0;
+    const bool half_unit = NT == 2 && (int)blockIdx.x >= npair;
+    const bool single = NT == 1 || half_unit;  // this CTA has one Q tile
+    const int split = half_unit ? 0 : (int)(blockIdx.x % (unsigned)S);
+    const int u = half_unit ? npair + ((int)blockIdx.x - npair) / 2 : (int)(blockIdx.x / (unsigned)S);
+    const int half = half_unit ? ((int)blockIdx.x - npair) & 1 : 0;
     const int g0 = (u / (G * nqb)) * G;
     const int gh = min(G, BH - g0);
     const int r = u - g0 * nqb;
     const long bh = g0 + r % gh;
     const int qblk = nqb - 1 - r / gh;
-    const int q0 = qblk * 2 * BM + half * BM;
+    const int q0 = qblk * NT * BM + half * BM;
     const int hh = (int)(bh % H), bb = (int)(bh / H);  // head, batch (tensor-map coordinates)
     // This CTA covers key tiles [jb, jb + nk) of the ones its query block
     // needs (all of them when S = 1); n0, n1 count the tiles of that range each
@@ -234,7 +245,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(base + C::kTmemSlot, kTmemCols);
+        tmem_alloc(base + C::kTmemSlot, C::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -280,7 +291,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             for (int t = 0; t < 2; ++t)
                 if ((t == 0 ? n0 : n1) > 0) mbar_wait_bounded(bar(C::QF(t)), 0, nullptr, kWaitLimitNs);
         }
-    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    } else if (warp >= kMmaWarp && warp < kMmaWarp + NT) {
         // -------------------------------------------------------- MMA issuer of tile t
         // The whole warp runs this code with the same values in every lane;
         // one elected lane issues each MMA and commit.
@@ -557,7 +568,7 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
@@ -577,25 +588,31 @@ __global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
     if (!ok && threadIdx.x == 0) atomicExch(status, kDevStatusTimeout);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int NT>
 cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                       int num_sms, cudaStream_t st) {
-    using Cf = Cfg<D>;
-    auto kern = attn_bf16_tc_kernel<D, CAUSAL>;
+    using Cf = Cfg<D, NT>;
+    auto kern = attn_bf16_tc_kernel<D, CAUSAL, NT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int nqb = (p.N + 2 * BM - 1) / (2 * BM);
+    // the whole unified L1 / shared memory as shared memory, so two CTAs fit an SM
+    if (Cf::kMinBlocks > 1) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+    }
+    const int nqb = (p.N + NT * BM - 1) / (NT * BM);
     const int BH = p.B * p.H;
-    // heads per group: enough query blocks to keep every SM busy about twice over
-    int G = (2 * num_sms + nqb - 1) / nqb;
+    const int slots = num_sms * Cf::kMinBlocks;  // CTAs resident at once
+    // heads per group: enough query blocks to keep every CTA slot busy about twice over
+    int G = (2 * slots + nqb - 1) / nqb;
     G = G < 1 ? 1 : (G > BH ? BH : G);
     const int S = p.num_splits > 1 ? p.num_splits : 1;
     const long units = (long)nqb * BH;
     long npair = units * S, ncta = npair;
-    // Without the causal mask every unit takes the same time, so a last wave
-    // of k < SMs/2 units would leave most SMs idle: those k units run as 2k
-    // single-tile CTAs instead, each about 0.6 of a unit's time.
-    if (S == 1 && !CAUSAL) {
+    // Two-tile CTAs without the causal mask all take the same time, so a last
+    // wave of k < SMs/2 units would leave most SMs idle: those k units run as
+    // 2k single-tile CTAs instead, each about 0.6 of a unit's time.
+    if (NT == 2 && S == 1 && !CAUSAL) {
         const long k = units % num_sms;
         if (units >= num_sms && k > 0 && 2 * k <= num_sms) {
             npair = units - k;
@@ -605,9 +622,9 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtenso
     const dim3 grid((unsigned)ncta);
     const float c_log2 = p.scale * 1.4426950408889634f;
     const int coff = p.causal == 2 ? p.M - p.N : 0;
-    kern<<<grid, kThreads, Cf::kSmemBytes, st>>>(*tmQ, *tmK, *tmV, p.O, p.LSE, p.N, p.M, c_log2, p.out_bf16, p.status,
-                                                 nqb, BH, G, S, p.Opart, p.Lpart, p.H, coff, p.os[0], p.os[1],
-                                                 p.os[2], (int)npair);
+    kern<<<grid, Cf::kThreads, Cf::kSmemBytes, st>>>(*tmQ, *tmK, *tmV, p.O, p.LSE, p.N, p.M, c_log2, p.out_bf16,
+                                                     p.status, nqb, BH, G, S, p.Opart, p.Lpart, p.H, coff, p.os[0],
+                                                     p.os[1], p.os[2], (int)npair);
     return cudaGetLastError();
 }
 
@@ -616,11 +633,11 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtenso
 cudaError_t launch_attn_bf16_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                 const CUtensorMap* tmV, int num_sms, cudaStream_t st) {
     if (p.d == 64)
-        return p.causal ? launch_tc<64, true>(p, tmQ, tmK, tmV, num_sms, st)
-                        : launch_tc<64, false>(p, tmQ, tmK, tmV, num_sms, st);
+        return p.causal ? launch_tc<64, true, 1>(p, tmQ, tmK, tmV, num_sms, st)
+                        : launch_tc<64, false, 1>(p, tmQ, tmK, tmV, num_sms, st);
     if (p.d == 128)
-        return p.causal ? launch_tc<128, true>(p, tmQ, tmK, tmV, num_sms, st)
-                        : launch_tc<128, false>(p, tmQ, tmK, tmV, num_sms, st);
+        return p.causal ? launch_tc<128, true, 2>(p, tmQ, tmK, tmV, num_sms, st)
+                        : launch_tc<128, false, 2>(p, tmQ, tmK, tmV, num_sms, st);
     return cudaErrorInvalidValue;
 }
 
