@@ -86,7 +86,7 @@ struct Cfg {
     static constexpr uint32_t kBar = kSlot + 2 * NSL * kTileBytes;  // mbarriers
     // d = 64: P has tensor-memory columns of its own (see the file comment)
     static constexpr bool kSepP = D == 64;
-    static constexpr int kNumBars = 15 + 3 * NSL;
+    static constexpr int kNumBars = 17 + 3 * NSL;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kSmemBytes = kAbort + 4 + 1024;    // + slack to align the base
@@ -103,6 +103,9 @@ struct Cfg {
     // separate-P mode: S_t read into registers (SC), P_t V done (PD)
     __host__ __device__ static constexpr int SC(int t) { return 11 + 3 * NSL + t; }
     __host__ __device__ static constexpr int PD(int t) { return 13 + 3 * NSL + t; }
+    // P-over-S mode: the first half of P_t (keys 0-63) stored; PF then means
+    // the second half
+    __host__ __device__ static constexpr int PH(int t) { return 15 + 3 * NSL + t; }
     // tensor-memory columns: S_t, then O_t, then (d = 64) P_t
     __host__ __device__ static constexpr uint32_t colS(int t) { return (uint32_t)t * 128u; }
     __host__ __device__ static constexpr uint32_t colO(int t) { return NT * 128u + (uint32_t)t * D; }
@@ -221,7 +224,8 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     if (warp == kLoadWarp && lane == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == C::PF(0) || i == C::PF(1) || i == C::SC(0) || i == C::SC(1))
+            if (i == C::PF(0) || i == C::PF(1) || i == C::SC(0) || i == C::SC(1) || i == C::PH(0) ||
+                i == C::PH(1))
                 count = BM;  // one arrival per softmax thread
             mbar_init(bar(i), count);
         }
@@ -318,12 +322,15 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 mma_ss_elect(tS, dQ + off, kb + off, idS, kk > 0 ? 1u : 0u);
             }
         };
-        // O_t (+)= P_t V, V in ring slot sl, P_t (bf16, 64 columns) at tP
-        auto issue_PV = [&](int sl, uint32_t acc_first) {
+        // O_t (+)= P_t V over keys [16 k0, 16 k1) of the tile, V in ring slot
+        // sl, P_t (bf16, 64 columns) at tP
+        auto issue_PV = [&](int sl, uint32_t acc_first, int k0 = 0, int k1 = BN / 16) {
             const uint64_t vb = dV + (uint32_t)sl * kSlotStep;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-                mma_ts_elect(tO, tP + (uint32_t)kk * 8u, vb + (uint32_t)kk * 128u, idO, kk > 0 ? 1u : acc_first);
+                if (kk >= k0 && kk < k1)
+                    mma_ts_elect(tO, tP + (uint32_t)kk * 8u, vb + (uint32_t)kk * 128u, idO,
+                                 kk > 0 ? 1u : acc_first);
         };
         auto wait_all = [&](int b, uint32_t parity) -> bool {
             return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(b), parity, abort_flag, kWaitLimitNs));
@@ -365,10 +372,16 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 mma_commit_elect(bar(C::PD(t)));
                 if (j + 1 == n) mma_commit_elect(bar(C::OD(t)));
             } else {
-                ok = wait_all(C::FULL(sl), ph) && wait_all(C::PF(t), pj);
+                // P V over the first 64 keys as soon as that half of P is
+                // stored, the rest once all of it is
+                ok = wait_all(C::FULL(sl), ph) && wait_all(C::PH(t), pj);
                 if (!ok) break;
                 tc_fence_after();
-                issue_PV(sl, j > 0 ? 1u : 0u);
+                issue_PV(sl, j > 0 ? 1u : 0u, 0, BN / 32);
+                ok = wait_all(C::PF(t), pj);
+                if (!ok) break;
+                tc_fence_after();
+                issue_PV(sl, 1u, BN / 32, BN / 16);
                 if (j + 1 < n) {
                     issue_S(dK + (uint32_t)sl * kSlotStep);
                     mma_commit_elect(bar(C::SF(t)));
@@ -455,12 +468,39 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
             uint32_t pk[64];
+            auto exp_pairs = [&](int c0, int c1) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float2 t2 = fma2(make_float2(sv[2 * c], sv[2 * c + 1]), cc, nm);
-                const float2 p2 = make_float2(ex2(t2.x), ex2(t2.y));
-                ls[c & 3] = add2(ls[c & 3], p2);
-                pk[c] = pack_bf16x2(p2.x, p2.y);
+                for (int c = 0; c < 64; ++c) {
+                    if (c < c0 || c >= c1) continue;
+                    const float2 t2 = fma2(make_float2(sv[2 * c], sv[2 * c + 1]), cc, nm);
+                    const float2 p2 = make_float2(ex2(t2.x), ex2(t2.y));
+                    ls[c & 3] = add2(ls[c & 3], p2);
+                    pk[c] = pack_bf16x2(p2.x, p2.y);
+                }
+            };
+            if constexpr (!C::kSepP) {
+                // P over S: the first 64 keys' P goes out first (after any
+                // rescale of o~, which must precede every P V of this step)
+                // so the issuer can start P V while the rest is exponentiated
+                exp_pairs(0, 32);
+                if (__any_sync(0xFFFFFFFFu, rescale)) {
+                    // 16 columns at a time: half the exponentials' registers are live here
+#pragma unroll 1
+                    for (int ch = 0; ch < D / 16; ++ch) {
+                        uint32_t r[16];
+                        tmem_ld_x16(tO + ch * 16, r);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+                        tmem_st_x16(tO + ch * 16, r);
+                    }
+                }
+                tmem_st_x32(tP, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(C::PH(t)));
+                exp_pairs(32, 64);
+            } else {
+                exp_pairs(0, 64);
             }
             const float2 lsum = add2(add2(ls[0], ls[1]), add2(ls[2], ls[3]));
             l = fmaf(l, alpha, lsum.x + lsum.y);
@@ -477,12 +517,14 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     tc_fence_after();
                 }
             }
-            tmem_st_x64(tP, pk);
+            if constexpr (C::kSepP) tmem_st_x64(tP, pk);
+            else tmem_st_x32(tP + 32, pk + 32);
             // o~ <- alpha o~ when the reference max was raised.  The previous
             // P V of this tile has completed: with P over S it was issued
-            // before the Q K^T whose completion this warpgroup waited for, with
-            // P apart the PD wait above saw it done.
-            if (__any_sync(0xFFFFFFFFu, rescale)) {
+            // before the Q K^T whose completion this warpgroup waited for (and
+            // o~ was rescaled above, before the first half of P), with P apart
+            // the PD wait above saw it done.
+            if (C::kSepP && __any_sync(0xFFFFFFFFu, rescale)) {
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t r[32];
