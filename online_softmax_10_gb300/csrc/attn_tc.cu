@@ -86,6 +86,11 @@ struct Cfg {
     static constexpr uint32_t kBar = kSlot + 2 * NSL * kTileBytes;  // mbarriers
     // d = 64: P has tensor-memory columns of its own (see the file comment)
     static constexpr bool kSepP = D == 64;
+    // d = 64: the row max of each score tile comes with its tensor-memory load
+    // (tcgen05.ld.red); at d = 128 that form made every key step slower than
+    // the plain load followed by the max in registers (measured), so it keeps
+    // the latter
+    static constexpr bool kHwMax = D == 64;
     static constexpr int kNumBars = 17 + 3 * NSL;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
@@ -419,7 +424,9 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
             tc_fence_after();
             uint32_t sr[128];
-            tmem_ld_x128(tS, sr);
+            float hw_max = 0.f;  // row max of the 128 raw scores, from the load itself
+            if constexpr (C::kHwMax) tmem_ld_max_x128(tS, sr, hw_max);
+            else tmem_ld_x128(tS, sr);
             bool pd_ready = true;  // the previous P V of this tile is done (separate-P mode)
             if constexpr (C::kSepP) {
                 // S_t is in registers: the tile's next Q K^T may overwrite it
@@ -432,23 +439,27 @@ attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
             const int k0 = (jb + j) * BN;
             const bool need_mask = (k0 + BN > M) || (CAUSAL && k0 + BN - 1 > q0 + t * BM + coff);
+            float row_max = hw_max;
             if (need_mask) {
+                // masked keys (past M, or above the causal diagonal) become -inf
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     const int key = k0 + c;
                     if (key >= M || (CAUSAL && key > qi + coff)) sv[c] = -CUDART_INF_F;
                 }
             }
-            // row max: three-input max over eight independent chains
-            float mx[8];
+            if (need_mask || !C::kHwMax) {
+                // row max in registers: three-input max over eight independent chains
+                float mx[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[2 * i], sv[2 * i + 1]);
+                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[2 * i], sv[2 * i + 1]);
 #pragma unroll
-            for (int c = 16; c < 128; c += 16)
+                for (int c = 16; c < 128; c += 16)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = max3f(mx[i], sv[c + 2 * i], sv[c + 2 * i + 1]);
-            const float m_tile =
-                max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c_log2;
+                    for (int i = 0; i < 8; ++i) mx[i] = max3f(mx[i], sv[c + 2 * i], sv[c + 2 * i + 1]);
+                row_max = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            }
+            const float m_tile = row_max * c_log2;
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
