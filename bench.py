@@ -563,13 +563,19 @@ def run_only(args):
     from online_softmax_10_gb300 import fattn, inputs
     fbuild.build()
     torch.cuda.set_device(0)
-    if args.only == "attn":
+    if args.only in ("attn", "splitkv"):
         B, H, N, M, d, causal = (int(x) for x in args.shape.split(","))
         dt = torch.float32 if args.f32 else torch.bfloat16
         q, k, v = (t.cuda() for t in inputs.attn_inputs(B, H, N, M, d, dt, seed=3))
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
-        fn = lambda: fattn.attn_fwd(q, k, v, 1.0 / math.sqrt(d), bool(causal), out=o, lse=lse)
+        if args.only == "attn":
+            fn = lambda: fattn.attn_fwd(q, k, v, 1.0 / math.sqrt(d), bool(causal), out=o, lse=lse)
+        else:
+            S = fattn.splitkv_num_splits(B, H, N, M, d, bool(causal))
+            ws = torch.empty(max(1, fattn.splitkv_workspace_bytes(B, H, N, d, S)), dtype=torch.uint8, device="cuda")
+            fn = lambda: fattn.attn_fwd_splitkv(q, k, v, 1.0 / math.sqrt(d), bool(causal), num_splits=S,
+                                                workspace=ws, out=o, lse=lse)
         work = 4.0 * B * H * N * M * d / (2 if causal else 1)
         unit, scale = "TFLOP/s", 1e12
     else:
@@ -610,9 +616,9 @@ def main():
                     help="ncu dram bytes per attention launch, if captured for the current kernel")
     ap.add_argument("--rows-traffic", type=float, default=None,
                     help="ncu dram bytes per row-softmax launch, if captured for the current kernel")
-    ap.add_argument("--only", choices=["attn", "rows", "lse"], default=None,
+    ap.add_argument("--only", choices=["attn", "splitkv", "rows", "lse"], default=None,
                     help="time one kernel on --shape only (profiling aid; not the contract line)")
-    ap.add_argument("--shape", default=None, help="attn: B,H,N,M,d,causal   rows/lse: rows,cols")
+    ap.add_argument("--shape", default=None, help="attn/splitkv: B,H,N,M,d,causal   rows/lse: rows,cols")
     ap.add_argument("--f32", action="store_true", help="with --only attn: fp32 inputs")
     args = ap.parse_args()
     if args.warmup < 3:
