@@ -1062,6 +1062,197 @@ bool try_launch_warp_rows(const TIn* X, TOut* P, float* LSE, long rows, long col
     return true;
 }
 
+// ------------------------------------------------------------------ cluster per row
+// Rows longer than one CTA's registers hold (above 64 KB): a cluster of CL
+// CTAs (2 to 8) takes each row, CTA c holding the c-th of CL equal slices
+// (whole multiples of 256 vectors, at most 64 KB) packed in registers (256
+// threads x up to 16 vectors of 16 bytes).  Every CTA reduces its
+// slice to (m, s) (slice max first, one exponential per element relative to
+// it, then the pairwise online update across the CTA), stores that pair into
+// a slot of every CTA of the cluster through distributed shared memory and
+// arrives on each one's exchange barrier; once all CL pairs are in, every CTA
+// merges them in the same order to the row's (M, S) and writes its slice of P
+// (or log P) from registers.  X is read from memory once and P written once.
+// Slots and exchange barriers alternate between two sets by row parity: a CTA
+// reaches row k + 2 only after every CTA has arrived for row k + 1, which each
+// does after reading its row-k slots.  The row loop is the same in every CTA
+// of a cluster, so the two cluster-wide barriers (after set-up, before exit)
+// are reached by all.  Two CTAs per SM: one reduces while the other loads.
+// KIND: 0 softmax, 1 log-softmax, 2 log-sum-exp only (and / or the fused
+// cross-entropy loss).
+constexpr int kClThreads = 256;
+constexpr int kClNV = 16;      // 16-byte vectors per thread: a 64 KB slice per CTA
+constexpr int kClMaxCtas = 8;  // portable cluster size
+
+template <typename TIn, typename TOut, int KIND>
+__global__ void __launch_bounds__(kClThreads, 2)
+rows_cluster(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restrict__ LSE, long rows, long cols,
+             int* status, const long long* __restrict__ labels, float* __restrict__ loss) {
+    constexpr int V = Elem<TIn>::kVec;
+    constexpr int W = kClThreads / 32;
+    __shared__ __align__(8) uint64_t xbar[2];             // exchange barriers, by row parity
+    __shared__ __align__(8) float2 slots[2][kClMaxCtas];  // (m, s) of every CTA, by row parity
+    __shared__ float2 wred[W];
+    __shared__ int abort_flag;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t ncta = cluster_nctarank();
+    const long cid = cluster_id_x(), ncl = num_clusters_x();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&xbar[0]), ncta);
+        mbar_init(smem_u32(&xbar[1]), ncta);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    // every CTA's barriers exist before any CTA of the cluster arrives on them
+    cluster_sync_all();
+    const long nvec = cols / V;
+    // this CTA's vectors: [v0, v1), an equal share rounded up to whole rows of threads
+    const long per = ((nvec + ncta - 1) / ncta + kClThreads - 1) / kClThreads * kClThreads;
+    const long v0 = rank * per, v1 = v0 + per < nvec ? v0 + per : nvec;
+    constexpr uint32_t ni = neg_inf_word<TIn>();
+    const float2 cc = make_float2(kLog2e, kLog2e);
+    bool ok = true;
+    long k = 0;
+    for (long r = cid; r < rows; r += ncl, ++k) {
+        const TIn* xr = X + r * cols;
+        uint4 raw[kClNV];
+#pragma unroll
+        for (int kk = 0; kk < kClNV; ++kk) {
+            const long vi = v0 + (long)kk * kClThreads + threadIdx.x;
+            raw[kk] = vi < v1 ? __ldg(reinterpret_cast<const uint4*>(xr + vi * V)) : make_uint4(ni, ni, ni, ni);
+        }
+        // this thread: max, then the sum of exp(x - max)
+        float m = slice_max<TIn, kClNV>(raw);
+        float sum = 0.f;
+        if (m != -CUDART_INF_F) {
+            const float2 nmc = make_float2(-m * kLog2e, -m * kLog2e);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+#pragma unroll
+            for (int kk = 0; kk < kClNV; ++kk)
+#pragma unroll
+                for (int e = 0; e < (V == 8 ? 4 : 2); ++e) {
+                    const float2 t2 = fma2(unpack_pair<TIn>(raw[kk], e), cc, nmc);
+                    acc[e] = add2(acc[e], make_float2(ex2(t2.x), ex2(t2.y)));
+                }
+            const float2 a2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+            sum = a2.x + a2.y;
+        }
+        // the CTA's pair: warps by shuffles (max first, then the rescaled
+        // sums), then warp 0 over the W warp results
+        float wm = m;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+        float ws = wm == -CUDART_INF_F ? 0.f : sum * ex2((m - wm) * kLog2e);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, off);
+        if (lane == 0) wred[warp] = make_float2(wm, ws);
+        __syncthreads();
+        const int par = (int)(k & 1);
+        if (warp == 0) {
+            const float2 a = wred[lane & (W - 1)];
+            float M = a.x;
+#pragma unroll
+            for (int off = W / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+            float S = M == -CUDART_INF_F ? 0.f : a.y * ex2((a.x - M) * kLog2e);
+#pragma unroll
+            for (int off = W / 2; off > 0; off >>= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, off);
+            // lane t hands the pair to CTA t of the cluster
+            if ((uint32_t)lane < ncta) {
+                st_cluster_f32x2(mapa_shared(smem_u32(&slots[par][rank]), (uint32_t)lane), M, S);
+                mbar_arrive_cluster(mapa_shared(smem_u32(&xbar[par]), (uint32_t)lane));
+            }
+        }
+        ok = __syncthreads_and(mbar_wait_cluster_bounded(smem_u32(&xbar[par]), (uint32_t)(k >> 1) & 1u, &abort_flag,
+                                                         kWaitLimitNs));
+        if (!ok) break;
+        // the row's (M, S): every CTA merges the same pairs in the same order
+        float M = -CUDART_INF_F, S = 0.f;
+        for (uint32_t c = 0; c < ncta; ++c) {
+            const float2 q = slots[par][c];
+            merge_ms(M, S, q.x, q.y);
+        }
+        const float lse = M + __log2f(S) * kLn2f;
+        if constexpr (KIND < 2) {
+            TOut* pr = P + r * cols;
+            const float l2s = __log2f(S);
+#pragma unroll
+            for (int kk = 0; kk < kClNV; ++kk) {
+                const long vi = v0 + (long)kk * kClThreads + threadIdx.x;
+                if (vi >= v1) continue;
+                float f[V];
+#pragma unroll
+                for (int e = 0; e < V / 2; ++e) {
+                    const float2 x2 = unpack_pair<TIn>(raw[kk], e);
+                    if (!(S > 0.f)) {
+                        // a row with no finite entry: p = 0, log p = -inf (LSE = -inf)
+                        f[2 * e] = f[2 * e + 1] = KIND == 1 ? -CUDART_INF_F : 0.f;
+                    } else if constexpr (KIND == 1) {
+                        f[2 * e] = x2.x - lse;
+                        f[2 * e + 1] = x2.y - lse;
+                    } else {
+                        // p = 2^((x - M) log2 e - log2 S)
+                        f[2 * e] = ex2(fmaf(x2.x - M, kLog2e, -l2s));
+                        f[2 * e + 1] = ex2(fmaf(x2.y - M, kLog2e, -l2s));
+                    }
+                }
+                store_out<TOut, V>(pr + vi * V, f, true, V);
+            }
+        }
+        if (rank == 0 && threadIdx.x == 0) write_row_lse(X, r, cols, lse, LSE, labels, loss);
+    }
+    if (!ok && threadIdx.x == 0) {
+        abort_flag = 1;
+        atomicExch(status, kDevStatusTimeout);
+    }
+    // no CTA leaves while another CTA of the cluster may still write into its
+    // shared memory
+    cluster_sync_all();
+}
+
+// Launch the cluster-per-row kernel if the row shape suits it: whole 16-byte
+// vectors, more than one 64 KB slice and at most kClMaxCtas of them.  For the
+// log-sum-exp alone (nothing to write behind which the per-row exchange could
+// hide) only when each CTA's share is nearly a full slice and the cluster has
+// at most four CTAs; otherwise the streaming kernel, which keeps loads in
+// flight while it reduces, measured faster.
+template <typename TIn, typename TOut, int KIND>
+bool try_launch_cluster(const TIn* X, TOut* P, float* LSE, long rows, long cols, int* status, cudaStream_t st,
+                        cudaError_t* err, const long long* labels = nullptr, float* loss = nullptr) {
+    constexpr int V = Elem<TIn>::kVec;
+    constexpr long kSliceVec = (long)kClThreads * kClNV;
+    if (cols % V != 0) return false;
+    const long nvec = cols / V;
+    if (nvec <= kSliceVec || nvec > kClMaxCtas * kSliceVec) return false;
+    const int ncta = (int)((nvec + kSliceVec - 1) / kSliceVec);
+    if (KIND == 2 && (ncta > 4 || (nvec + ncta - 1) / ncta < (long)(kClNV - 1) * kClThreads)) return false;
+    auto kern = rows_cluster<TIn, TOut, KIND>;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ncta;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many clusters as fit the GPU at once (each loops over rows)
+    cfg.gridDim = dim3((unsigned)ncta);
+    int active = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
+    if (e != cudaSuccess || active < 1) {
+        *err = e != cudaSuccess ? e : cudaErrorLaunchOutOfResources;
+        return true;
+    }
+    const long ncl = rows < active ? rows : active;
+    cfg.gridDim = dim3((unsigned)(ncl * ncta));
+    *err = cudaLaunchKernelEx(&cfg, kern, X, P, LSE, rows, cols, status, labels, loss);
+    return true;
+}
+
 long grid_for_rows(long rows) {
     const long kMaxGrid = 1L << 30;
     return rows < kMaxGrid ? rows : kMaxGrid;
@@ -1074,6 +1265,7 @@ cudaError_t softmax_dispatch(const TIn* X, TOut* P, float* LSE, long rows, long 
     cudaError_t terr;
     if (try_launch_tma<TIn, TOut, true, LOGP>(X, P, LSE, rows, cols, status, st, &terr)) return terr;
     if (try_launch_warp_rows<TIn, TOut, LOGP ? 1 : 0>(X, P, LSE, rows, cols, st, &terr)) return terr;
+    if (try_launch_cluster<TIn, TOut, LOGP ? 1 : 0>(X, P, LSE, rows, cols, status, st, &terr)) return terr;
     const int vec_ok = (cols % V) == 0;
     const long nvec = (cols + V - 1) / V;
     const dim3 grid((unsigned)grid_for_rows(rows));
@@ -1098,6 +1290,7 @@ cudaError_t lse_dispatch(const TIn* X, float* LSE, long rows, long cols, int* st
     cudaError_t terr;
     if (try_launch_warp_rows<TIn, float, 2>(X, nullptr, LSE, rows, cols, st, &terr, labels, loss)) return terr;
     if (try_launch_lse_tma<TIn>(X, LSE, rows, cols, status, st, &terr, labels, loss)) return terr;
+    if (try_launch_cluster<TIn, float, 2>(X, nullptr, LSE, rows, cols, status, st, &terr, labels, loss)) return terr;
     const int vec_ok = (cols % V) == 0;
     const long nvec = (cols + V - 1) / V;
     const dim3 grid((unsigned)grid_for_rows(rows));

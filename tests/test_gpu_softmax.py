@@ -81,6 +81,32 @@ def test_logsumexp_shapes(cols, din):
     assert ok, rel
 
 
+@pytest.mark.parametrize("cols,din", [(32776, torch.bfloat16), (131072, torch.bfloat16), (229376, torch.bfloat16),
+                                      (262144, torch.bfloat16), (16388, torch.float32), (131072, torch.float32)])
+@pytest.mark.parametrize("dout", [torch.bfloat16, torch.float32])
+def test_cluster_rows(cols, din, dout):
+    """Rows above 64 KB of whole 16-byte vectors: a cluster of 2 to 8 CTAs per
+    row, each holding a 64 KB slice (the last one partly past the row end), the
+    row's (max, sum) exchanged through distributed shared memory; more rows
+    than clusters, so each cluster loops over rows (both exchange-slot sets)."""
+    rows = 400 if cols * (2 if din == torch.bfloat16 else 4) <= 300000 else 160
+    x = inputs.rows_inputs(rows, cols, din, seed=cols + rows)
+    p, lse = softmax(x.cuda(), out_dtype=dout)
+    lse2 = logsumexp(x.cuda())
+    y, lse3 = log_softmax(x.cuda(), out_dtype=torch.float32)
+    assert fattn.device_status() == fattn.FA_OK
+    sample = inputs.sample_rows(rows, 24, seed=cols).numpy()
+    _check(x, p, lse, sample)
+    sub = x[torch.as_tensor(sample)]
+    L_ref = oracle.logsumexp_rows(sub)
+    for got in (lse2, lse3):
+        ok, rel = lse_ok(to_np(got)[sample], L_ref)
+        assert ok, rel
+    Y, _ = oracle.log_softmax_rows(sub)
+    yg = to_np(y)[sample]
+    assert np.all(np.abs(yg - Y) <= 1e-5 + 1e-6 * np.abs(Y)), float(np.max(np.abs(yg - Y)))
+
+
 @pytest.mark.parametrize("rows", [64, 153, 1000])
 @pytest.mark.parametrize("cols,din", [(4096, torch.bfloat16), (6144, torch.bfloat16), (8192, torch.bfloat16),
                                       (16384, torch.bfloat16), (24576, torch.bfloat16), (32768, torch.bfloat16),
