@@ -12,11 +12,13 @@
 // "Softmax与Flash-Attention" page attributes to FlashAttention-2), so o~
 // stays on chip for the whole pass.
 //
-// Grid: one CTA per 256 query rows of one (batch, head), numbered so that the
-// hardware's in-order dispatch is a longest-first list schedule within groups
-// of heads: all query blocks of G heads (longest causal blocks first) before
-// the next G heads.  The group keeps the K/V tiles the in-flight CTAs share
-// resident in L2, and longest-first keeps the causal tail short.
+// Grid: one CTA per 256 query rows of one (batch, head) (128 rows at d = 64),
+// numbered so that the hardware's in-order dispatch is a longest-first list
+// schedule within groups of heads: all query blocks of G heads (longest causal
+// blocks first) before the next G heads.  The group keeps the K/V tiles the
+// in-flight CTAs share resident in L2, and longest-first keeps the causal tail
+// short; under the causal mask G is chosen by simulating that dispatch
+// (causal_group_heads).
 //
 // CTA organisation:
 //   warps 0-3  softmax warpgroup for Q tile 0 (rows q0 .. q0+127), one row per thread
@@ -50,6 +52,12 @@
 // tensor memory and exits.
 #include <cuda_bf16.h>
 #include <math_constants.h>
+
+#include <algorithm>
+#include <functional>
+#include <mutex>
+#include <queue>
+#include <vector>
 
 #include "fattn_internal.cuh"
 #include "ptx.cuh"
@@ -641,6 +649,80 @@ __global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
     if (!ok && threadIdx.x == 0) atomicExch(status, kDevStatusTimeout);
 }
 
+// Heads per group (G) for a causal launch.  CTAs are dispatched in index order,
+// each to the first free slot, and their lengths (key tiles) vary by query
+// block, so the order decides the tail: within a group of G heads the blocks
+// go longest first, and the last group's long CTAs can start too late.  This
+// simulates that dispatch for candidate G -- every divisor of B*H whose
+// group's K and V (2 * M * d * 2 bytes per head) stay within about the L2's
+// 128 MB, and the default -- and keeps the shortest makespan (the smaller G
+// when within 0.5 %, for L2 reuse).  Measured on the benchmark's causal
+// workloads: B2 H32 N=M=8192 d128 G 10 -> 16, 1543 -> 1600 TFLOP/s; B1 H16
+// N=M=32768 G 3 -> 8, 1740 -> 1797.  Choices are cached per shape.
+int causal_group_heads(int BH, int nqb, int N, int M, int d, int coff, int rows_per_cta, int slots, int G0) {
+    struct Key {
+        int BH, nqb, N, M, d, coff, rows, slots;
+        bool operator==(const Key& o) const {
+            return BH == o.BH && nqb == o.nqb && N == o.N && M == o.M && d == o.d && coff == o.coff &&
+                   rows == o.rows && slots == o.slots;
+        }
+    };
+    constexpr int kCache = 16;
+    static Key keys[kCache];
+    static int vals[kCache];
+    static int used = 0, next = 0;
+    static std::mutex mu;
+    const Key key{BH, nqb, N, M, d, coff, rows_per_cta, slots};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (keys[i] == key) return vals[i];
+    }
+    // key tiles of query block b: its last row's kept keys, in tiles of BN
+    const int nM = (M + BN - 1) / BN;
+    std::vector<int> len(nqb);
+    for (int b = 0; b < nqb; ++b) {
+        const long last = std::min((long)N, (long)(b + 1) * rows_per_cta) - 1 + coff;
+        len[b] = last < 0 ? 0 : (int)std::min((long)nM, last / BN + 1);
+    }
+    constexpr double kFixed = 3.0;  // set-up and epilogue, in key steps
+    auto makespan = [&](int G) {
+        std::priority_queue<double, std::vector<double>, std::greater<double>> freeq;
+        for (int i = 0; i < slots; ++i) freeq.push(0.0);
+        double end = 0.0;
+        const long units = (long)nqb * BH;
+        for (long u = 0; u < units; ++u) {
+            const int g0 = (int)(u / ((long)G * nqb)) * G;
+            const int gh = std::min(G, BH - g0);
+            const int r = (int)(u - (long)g0 * nqb);
+            const int qblk = nqb - 1 - r / gh;
+            const double t = freeq.top() + len[qblk] + kFixed;
+            freeq.pop();
+            freeq.push(t);
+            end = std::max(end, t);
+        }
+        return end;
+    };
+    const double kv_head = 2.0 * M * d * 2.0;
+    const int cap = std::max(1, (int)(128.0 * 1024 * 1024 / kv_head));
+    int best = G0;
+    double best_t = makespan(G0);
+    for (int g = 1; g <= std::min(BH, cap); ++g) {
+        if (BH % g != 0 || g == G0) continue;
+        const double t = makespan(g);
+        if (t < best_t * 0.995 || (t < best_t * 1.005 && g < best)) {
+            if (t < best_t) best_t = t;
+            best = g;
+        }
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    keys[next] = key;
+    vals[next] = best;
+    next = (next + 1) % kCache;
+    used = std::min(used + 1, kCache);
+    return best;
+}
+
 template <int D, bool CAUSAL, int NT>
 cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                       int num_sms, cudaStream_t st) {
@@ -660,6 +742,8 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtenso
     int G = (2 * slots + nqb - 1) / nqb;
     G = G < 1 ? 1 : (G > BH ? BH : G);
     const int S = p.num_splits > 1 ? p.num_splits : 1;
+    const int coff = p.causal == 2 ? p.M - p.N : 0;
+    if (CAUSAL && S == 1) G = causal_group_heads(BH, nqb, p.N, p.M, D, coff, NT * BM, slots, G);
     const long units = (long)nqb * BH;
     long npair = units * S, ncta = npair;
     // Two-tile CTAs without the causal mask all take the same time, so a last
@@ -674,7 +758,6 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtenso
     }
     const dim3 grid((unsigned)ncta);
     const float c_log2 = p.scale * 1.4426950408889634f;
-    const int coff = p.causal == 2 ? p.M - p.N : 0;
     kern<<<grid, Cf::kThreads, Cf::kSmemBytes, st>>>(*tmQ, *tmK, *tmV, p.O, p.LSE, p.N, p.M, c_log2, p.out_bf16,
                                                      p.status, nqb, BH, G, S, p.Opart, p.Lpart, p.H, coff, p.os[0],
                                                      p.os[1], p.os[2], (int)npair);
