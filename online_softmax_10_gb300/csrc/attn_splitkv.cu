@@ -9,8 +9,8 @@
 // A split that kept no key for a row has LSE_s = -inf and weight 0 (its o_s is
 // never read).  One warp per row; lane i owns the D/32 adjacent columns
 // [i D/32, (i+1) D/32), read as one 16-byte (d = 128) or 8-byte (d = 64)
-// load per split, and the splits are walked eight at a time so their loads are
-// in flight together instead of costing one memory latency each.
+// load per split, and the splits are walked sixteen at a time so their loads
+// are in flight together instead of costing one memory latency each.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -47,6 +47,7 @@ attn_combine_kernel(const float* __restrict__ Opart, const float* __restrict__ L
                     float* __restrict__ LSE, long rows, int S, int out_bf16, int N, int H, long long osb,
                     long long osh, long long osr) {
     constexpr int C = D / 32;  // adjacent columns per lane
+    constexpr int kBatch = 16; // splits whose loads are in flight together
     const int lane = threadIdx.x & 31;
     const long row = (long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
     if (row >= rows) return;
@@ -74,11 +75,11 @@ attn_combine_kernel(const float* __restrict__ Opart, const float* __restrict__ L
     for (int c = 0; c < C; ++c) acc[c] = 0.f;
     const float* base = Opart + row * D + lane * C;
     const long sstride = rows * D;  // floats between one split's partials and the next
-    for (int s0 = 0; s0 < S; s0 += 8) {
-        float v[8][C];
-        float w[8];
+    for (int s0 = 0; s0 < S; s0 += kBatch) {
+        float v[kBatch][C];
+        float w[kBatch];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kBatch; ++k) {
             const int sidx = s0 + k;
             // LSE_s from the lane that holds it (uniform shuffle source)
             const float l = __shfl_sync(0xFFFFFFFFu, ((sidx >> 5) & 1) ? ls[1] : ls[0], sidx & 31);
@@ -90,7 +91,7 @@ attn_combine_kernel(const float* __restrict__ Opart, const float* __restrict__ L
             }
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < kBatch; ++k)
 #pragma unroll
             for (int c = 0; c < C; ++c) acc[c] = fmaf(w[k], v[k][c], acc[c]);
     }

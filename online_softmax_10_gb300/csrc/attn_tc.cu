@@ -54,6 +54,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <atomic>
 #include <functional>
 #include <mutex>
 #include <queue>
@@ -728,12 +729,21 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* tmQ, const CUtenso
                       int num_sms, cudaStream_t st) {
     using Cf = Cfg<D, NT>;
     auto kern = attn_bf16_tc_kernel<D, CAUSAL, NT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmemBytes);
+    // kernel attributes: set once per device (one bit per device number)
+    static std::atomic<uint64_t> attrs_set{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    // the whole unified L1 / shared memory as shared memory, so two CTAs fit an SM
-    if (Cf::kMinBlocks > 1) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+    if (bit == 0 || (attrs_set.load() & bit) == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmemBytes);
         if (e != cudaSuccess) return e;
+        // the whole unified L1 / shared memory as shared memory, so two CTAs fit an SM
+        if (Cf::kMinBlocks > 1) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+            if (e != cudaSuccess) return e;
+        }
+        attrs_set.fetch_or(bit);
     }
     const int nqb = (p.N + NT * BM - 1) / (NT * BM);
     const int BH = p.B * p.H;

@@ -34,6 +34,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <mutex>
+
 #include "fattn_internal.cuh"
 #include "ptx.cuh"
 
@@ -1239,13 +1241,31 @@ bool try_launch_cluster(const TIn* X, TOut* P, float* LSE, long rows, long cols,
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // as many clusters as fit the GPU at once (each loops over rows)
+    // as many clusters as fit the GPU at once (each loops over rows); the
+    // occupancy query is a driver call, so its answer is kept per device and
+    // cluster size
     cfg.gridDim = dim3((unsigned)ncta);
-    int active = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
-    if (e != cudaSuccess || active < 1) {
-        *err = e != cudaSuccess ? e : cudaErrorLaunchOutOfResources;
+    static int active_cache[64][kClMaxCtas + 1] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *err = e;
         return true;
+    }
+    int active = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 0 && dev < 64) active = active_cache[dev][ncta];
+    }
+    if (active == 0) {
+        e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
+        if (e != cudaSuccess || active < 1) {
+            *err = e != cudaSuccess ? e : cudaErrorLaunchOutOfResources;
+            return true;
+        }
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 0 && dev < 64) active_cache[dev][ncta] = active;
     }
     const long ncl = rows < active ? rows : active;
     cfg.gridDim = dim3((unsigned)(ncl * ncta));
