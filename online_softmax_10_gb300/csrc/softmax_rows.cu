@@ -35,6 +35,7 @@
 #include <math_constants.h>
 
 #include <mutex>
+#include <unordered_map>
 
 #include "fattn_internal.cuh"
 #include "ptx.cuh"
@@ -444,8 +445,112 @@ constexpr int kTmaConsumers = 512;                 // 16 consumer warps
 constexpr int kTmaThreads = kTmaConsumers + 32;    // + 1 producer warp
 constexpr int kTmaMaxStages = 8;
 constexpr uint32_t kTmaSmemBudget = 200 * 1024;
-constexpr uint32_t kTmaBarBytes = 256;             // full[8], empty[8], red[4]
+constexpr uint32_t kTmaBarBytes = 384;             // full[8], empty[8], red[4], rowq[16]
 constexpr uint32_t kTmaSmemExtra = 128 /* alignment */ + kTmaBarBytes + 2 * 16 * 8 /* (m, s) slots */ + 16;
+// With tail rows the barrier area also holds the row index of each item in
+// the ring, after red[4]: item i's in rowq[i % kRowq].  The producer writes
+// item i + kRowq's entry only once item i + kRowq - nst has been taken, and
+// that item belongs to the same consumer group as item i (nst and kRowq are
+// multiples of the group count) and comes after it, so a group may read its
+// item's entry again until the end of that item.
+constexpr int kRowq = 16;
+constexpr uint32_t kTmaRowqOffset = 8u * (2 * kTmaMaxStages + 4);
+static_assert(kTmaRowqOffset + 8u * kRowq <= kTmaBarBytes, "barrier area");
+static_assert(kRowq > kTmaMaxStages && kRowq % 4 == 0, "row index ring");
+
+// ------------------------------------------------------------------ tail rows
+// Under full load the SMs do not stream at one rate (the row count an SM gets
+// through in a fixed time varies by about +-8 %), so with a purely static
+// split the slowest SM's rows set the end of the kernel.  The LSE kernel on
+// rows above 16 KB therefore takes its first rounds of rows statically (row
+// blockIdx.x + j * gridDim.x) and the last kTailRounds rounds of 64 KB per CTA
+// a chunk of rows per request from a counter, so that the faster SMs take more
+// of the tail.
+//
+// A counter is one word of g_tail_ctr, (CTAs done << 32) | next row; it is
+// zero when a launch starts.  Every CTA requests rows until the range is
+// exhausted, then counts itself done; the CTA that counts gridDim.x zeroes
+// the word again.  Each stream has a word of its own, so launches that share
+// a word run one after another (see launch_tail).
+constexpr int kTailSlots = 256;
+constexpr int kTailRounds = 8;
+__device__ unsigned long long g_tail_ctr[kTailSlots];
+
+// The producer lane of the pipelined LSE kernel with tail rows: rows into the
+// ring of `nst` stages (item i's row index in rowq[i % kRowq]), then one end
+// marker (row -1) per consumer group, so that every group's last item is its
+// marker.  `tail`: the launch's counter (null: a static split of every row).
+template <typename TIn>
+__device__ __forceinline__ void produce_rows(const TIn* __restrict__ X, long rows, long cols, uint32_t base,
+                                             uint32_t stage_bytes, int nst, int ng, uint32_t bar0, long long* rowq,
+                                             volatile int* abort_flag, int* status,
+                                             unsigned long long* __restrict__ tail) {
+    const uint64_t pol = l2_policy_evict_first();  // every row is read exactly once
+    const uint32_t row_bytes = (uint32_t)(cols * (long)sizeof(TIn));
+    long issued = 0;
+    bool live = true;
+    // one item into the next stage: a row, or an end marker (r < 0)
+    auto push = [&](long r) {
+        if (!live) return;
+        const int s = (int)(issued % nst);
+        const uint32_t ph = (uint32_t)(issued / nst) & 1u;
+        const uint32_t fb = bar0 + 8u * (uint32_t)s;
+        if (!mbar_wait_bounded(bar0 + 8u * (uint32_t)(kTmaMaxStages + s), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+            *abort_flag = 1;
+            atomicExch(status, kDevStatusTimeout);
+            live = false;
+            return;
+        }
+        rowq[issued % kRowq] = r;
+        ++issued;
+        if (r < 0) {
+            mbar_arrive(fb);
+            return;
+        }
+        mbar_expect_tx(fb, row_bytes);
+        const char* src = reinterpret_cast<const char*>(X + r * cols);
+        const uint32_t dst = base + (uint32_t)s * stage_bytes;
+        for (uint32_t off = 0; off < row_bytes; off += 32768u) {
+            const uint32_t n = row_bytes - off < 32768u ? row_bytes - off : 32768u;
+            bulk_load(dst + off, src + off, n, fb, pol);
+        }
+    };
+    const long G = gridDim.x, b = blockIdx.x;
+    if (tail == nullptr) {
+        for (long r = b; r < rows; r += G) push(r);
+    } else {
+        // a request takes c consecutive rows (about 64 KB, so that the
+        // request's round trip stays below the time the rows take); static
+        // rounds: all whole rounds but the last kTailRounds * c, and at least
+        // the ring's depth; then chunks n of rows r0 + n c .. on request
+        const long c = row_bytes >= 65536u ? 1 : 65536 / (long)row_bytes;
+        const long per = rows / G;
+        long ns = per - kTailRounds * c;
+        if (ns < (per < nst ? per : nst)) ns = per < nst ? per : nst;
+        const long r0 = ns * G, nd = (rows - r0 + c - 1) / c;
+        if (nd > 0) {
+            unsigned long long nxt = atomicAdd(tail, 1ull);  // one request ahead
+            for (long j = 0; j < ns; ++j) push(b + j * G);
+            for (;;) {
+                const long n = (long)(uint32_t)nxt;
+                if (n >= nd || !live) break;
+                nxt = atomicAdd(tail, 1ull);
+                const long e = r0 + (n + 1) * c < rows ? r0 + (n + 1) * c : rows;
+                for (long r = r0 + n * c; r < e; ++r) push(r);
+            }
+            // (also after a timeout: the word must be zero for the next launch)
+            const unsigned long long done = atomicAdd(tail, 1ull << 32);
+            if ((long)(done >> 32) == G - 1) atomicExch(tail, 0ull);
+        } else {
+            for (long j = 0; j < ns; ++j) push(b + j * G);
+        }
+    }
+    for (int g = 0; g < ng; ++g) push(-1);
+    // drain: the copies this thread issued have landed before it exits
+    for (long i = issued - nst < 0 ? 0 : issued - nst; i < issued; ++i)
+        mbar_wait_bounded(bar0 + 8u * (uint32_t)(i % nst), (uint32_t)(i / nst) & 1u, nullptr, kWaitLimitNs);
+}
+
 
 // One CTA per SM; rows r = blockIdx.x + i * gridDim.x go through a ring of
 // `nst` shared-memory stages of `stage_bytes` each.  The 16 consumer warps
@@ -684,10 +789,13 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
 // per element relative to it.
 // NG consumer groups: two of 8 warps for rows above 16 KB, four of 4 warps for
 // rows of 8-16 KB.
-template <typename TIn, int NV, int NG>
+// TAIL: the last rounds of rows come from the launch's counter `tail` (see
+// produce_rows); the ring then carries each item's row index.
+template <typename TIn, int NV, int NG, bool TAIL>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows, long cols, uint32_t stage_bytes,
-                   int nst, int* status, const long long* __restrict__ labels, float* __restrict__ loss) {
+                   int nst, int* status, const long long* __restrict__ labels, float* __restrict__ loss,
+                   unsigned long long* __restrict__ tail) {
     constexpr int V = Elem<TIn>::kVec;
     constexpr int GT = kTmaConsumers / NG;     // threads per group
     constexpr int WG = GT / 32;                // warps per group
@@ -718,7 +826,13 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
     }
     __syncthreads();
 
+    long long* rowq = reinterpret_cast<long long*>(gbase + (uint32_t)nst * stage_bytes + kTmaRowqOffset);
     if (warp == kTmaConsumers / 32) {
+        if constexpr (TAIL) {
+            if (lane == 0)
+                produce_rows<TIn>(X, rows, cols, base, stage_bytes, nst, NG, bar0, rowq, abort_flag, status, tail);
+            return;
+        }
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             long issued = 0;
@@ -749,8 +863,9 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
     const int gt = threadIdx.x % GT;                // thread within the group
     const float2 cc = make_float2(kLog2e, kLog2e);
     long k = 0;                                     // rows this group has done
-    for (long i = g; blockIdx.x + i * (long)gridDim.x < rows; i += NG, ++k) {
-        const long r = blockIdx.x + i * (long)gridDim.x;
+    // (static split: item i is row blockIdx.x + i * gridDim.x; with TAIL the
+    // ring holds each item's row, and a row < 0 ends the group's work)
+    for (long i = g; TAIL || blockIdx.x + i * (long)gridDim.x < rows; i += NG, ++k) {
         const int s = (int)(i % nst);
         const uint32_t ph = (uint32_t)(i / nst) & 1u;
         bool ok = mbar_wait_bounded(full(s), ph, abort_flag, kWaitLimitNs);
@@ -760,6 +875,7 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
             atomicExch(status, kDevStatusTimeout);
             break;
         }
+        if (TAIL && rowq[i % kRowq] < 0) break;
         // this thread's slice, still packed, into registers; the stage goes
         // back to the producer as soon as it is loaded
         const TIn* srow = reinterpret_cast<const TIn*>(gbase + (uint32_t)s * stage_bytes);
@@ -855,7 +971,10 @@ logsumexp_rows_tma(const TIn* __restrict__ X, float* __restrict__ LSE, long rows
             float S = M == -CUDART_INF_F ? 0.f : a.y * ex2((a.x - M) * kLog2e);
 #pragma unroll
             for (int off = WG / 2; off > 0; off >>= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, off);
-            if (lane == 0) write_row_lse(X, r, cols, M + __log2f(S) * kLn2f, LSE, labels, loss);
+            if (lane == 0) {
+                const long r = TAIL ? (long)rowq[i % kRowq] : blockIdx.x + i * (long)gridDim.x;
+                write_row_lse(X, r, cols, M + __log2f(S) * kLn2f, LSE, labels, loss);
+            }
         }
     }
 }
@@ -865,6 +984,69 @@ int device_sms() {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     return n > 0 ? n : 1;
+}
+
+// Counter slots for the tail rows, per device: each CUDA stream (by its id,
+// which a context never reuses) gets a slot of its own the first time it
+// launches the LSE kernel with tail rows, and keeps it.  Launches on one stream run one
+// after another, each starting with the word its predecessor zeroed, so a
+// slot never serves two launches at once.  Streams beyond kTailSlots keep the
+// static split.
+struct TailSlots {
+    std::mutex mu;
+    bool ready = false;
+    unsigned long long* words = nullptr;  // device address of g_tail_ctr
+    std::unordered_map<unsigned long long, int> slot_of;  // stream id -> slot
+};
+constexpr int kTailMaxDevices = 64;
+
+// Run `launch(tail)` with the stream's counter when the caller wants tail rows
+// (`want`), the input is at least 16 MB and the stream is not being captured
+// (the replays of a captured graph could overlap launches on the stream);
+// otherwise `launch(nullptr)`, a static split.  Returns the launch's error.
+template <typename F>
+cudaError_t launch_tail(cudaStream_t st, bool want, long rows, long row_bytes, F&& launch) {
+    if (!want || rows * row_bytes < (16L << 20)) return launch(nullptr);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return launch(nullptr);
+    }
+    if (cs != cudaStreamCaptureStatusNone) return launch(nullptr);  // (no other query on a capturing stream)
+    // (relaxed capture mode for the queries below, so that they cannot upset a
+    // capture that another thread runs in global mode)
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    unsigned long long sid = 0;
+    int dev = -1;
+    const bool ok = cudaStreamGetId(st, &sid) == cudaSuccess && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 &&
+                    dev < kTailMaxDevices;
+    static TailSlots slots[kTailMaxDevices];
+    unsigned long long* tail = nullptr;
+    if (ok) {
+        TailSlots& ts = slots[dev];
+        std::lock_guard<std::mutex> lock(ts.mu);
+        if (!ts.ready) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_tail_ctr) == cudaSuccess) {
+                ts.words = static_cast<unsigned long long*>(p);
+                ts.ready = true;
+            }
+        }
+        if (ts.ready) {
+            auto it = ts.slot_of.find(sid);
+            if (it != ts.slot_of.end()) {
+                tail = ts.words + it->second;
+            } else if ((int)ts.slot_of.size() < kTailSlots) {
+                const int k = (int)ts.slot_of.size();
+                ts.slot_of.emplace(sid, k);
+                tail = ts.words + k;
+            }
+        }
+    }
+    (void)cudaGetLastError();  // (a failed query above is not the launch's error)
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    return launch(tail);
 }
 
 // Launch the pipelined kernel if the row shape suits it; returns false if not.
@@ -925,22 +1107,32 @@ bool try_launch_lse_tma(const TIn* X, float* LSE, long rows, long cols, int* sta
     nst -= nst % ng;  // stage s belongs to consumer group s % ng
     const uint32_t smem = (uint32_t)nst * stage + kTmaSmemExtra;
     const long grid = rows < device_sms() ? rows : device_sms();
-    auto launch = [&](auto kern) {
+    auto launch = [&](auto kern, unsigned long long* tail) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess) {
-            kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(X, LSE, rows, cols, stage, nst, status, labels, loss);
+            kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(X, LSE, rows, cols, stage, nst, status, labels, loss,
+                                                             tail);
             e = cudaGetLastError();
         }
-        *err = e;
+        return e;
     };
     if (ng == 4) {
-        if (nvec <= 4L * (kTmaConsumers / 4)) launch(logsumexp_rows_tma<TIn, 4, 4>);
-        else launch(logsumexp_rows_tma<TIn, 8, 4>);
-    } else if (nvec <= 8L * (kTmaConsumers / 2)) {
-        launch(logsumexp_rows_tma<TIn, 8, 2>);
-    } else {
-        launch(logsumexp_rows_tma<TIn, 16, 2>);
+        // (rows up to 16 KB: a static split measured faster)
+        if (nvec <= 4L * (kTmaConsumers / 4)) *err = launch(logsumexp_rows_tma<TIn, 4, 4, false>, nullptr);
+        else *err = launch(logsumexp_rows_tma<TIn, 8, 4, false>, nullptr);
+        return true;
     }
+    // tail rows when the static rounds are at least half of every CTA's rows
+    // (fewer rounds: the requests cost more than the balance gains)
+    const long chunk = row_bytes >= 65536 ? 1 : 65536 / row_bytes;
+    const bool tail_ok = rows / grid >= 2L * kTailRounds * chunk;
+    *err = launch_tail(st, tail_ok, rows, row_bytes, [&](unsigned long long* tail) {
+        if (nvec <= 8L * (kTmaConsumers / 2))
+            return tail ? launch(logsumexp_rows_tma<TIn, 8, 2, true>, tail)
+                        : launch(logsumexp_rows_tma<TIn, 8, 2, false>, nullptr);
+        return tail ? launch(logsumexp_rows_tma<TIn, 16, 2, true>, tail)
+                    : launch(logsumexp_rows_tma<TIn, 16, 2, false>, nullptr);
+    });
     return true;
 }
 

@@ -1,0 +1,126 @@
+"""Run-time tail rows in the pipelined log-sum-exp kernel.
+
+Rows of 8-64 KB go through a persistent kernel with one CTA per SM.  For rows
+above 16 KB the LSE-only kernel takes its first rounds of rows statically and
+the last rounds a chunk of rows per request from a counter in device memory.
+Each CUDA stream gets a counter of its own, so launches that share a counter
+run one after another, and the last CTA of a launch zeroes it for the next.
+A row's arithmetic does not depend on the CTA that computes it, so every
+launch of the same input must give the same bits, and every row must be
+written: outputs start as NaN, so a row that no CTA took fails.  Checked
+(with the softmax kernel, which splits statically, on the same inputs) for
+launches back to back on one stream, for launches on four streams at once,
+and for the same calls captured once in a CUDA graph and replayed (a captured
+launch keeps the static split: the replays must still write every row, with
+the same bits as the direct launch); the first result of each case is
+compared with the fp64 oracle (LSE on every row, P on 64 sampled rows).
+Tolerances as in the row softmax tests: P max-abs 4e-3 (bf16) / 1e-5 (fp32),
+LSE relative 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from online_softmax_10_gb300 import fattn, inputs
+from parity import P_TOL_BF16, P_TOL_F32, ensure_built, lse_ok, nan_full, to_np
+
+pytestmark = pytest.mark.gpu
+
+# (rows, cols, input dtype): 64 KB rows (LSE: two consumer groups, tail rows
+# one per request), 32 KB (two rows per request), 12 KB (four groups, static)
+# and 64 KB fp32, ragged row counts; the tail is on when every CTA has at
+# least 16 rounds of 64 KB (152 SMs: 2432 rows of 64 KB, 4864 of 32 KB)
+SHAPES = [(2500, 32768, torch.bfloat16), (4900, 16384, torch.bfloat16), (2000, 6144, torch.bfloat16),
+          (2500, 16384, torch.float32), (16 * 152 + 3, 32768, torch.bfloat16)]
+P_SAMPLE = 64  # rows of P compared with the oracle (LSE: every row)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _oracle_check(x_cpu, p, lse, lse_only):
+    L_ref = oracle.logsumexp_rows(x_cpu)
+    for got in (lse, lse_only):
+        ok, rel = lse_ok(to_np(got), L_ref)
+        assert ok, rel
+    assert not torch.isnan(p).any().item(), "a row was never written"
+    rows = inputs.sample_rows(x_cpu.shape[0], P_SAMPLE, seed=x_cpu.shape[1]).numpy()
+    P_ref, _ = oracle.softmax_rows(x_cpu[torch.as_tensor(rows)])
+    pg = to_np(p[torch.as_tensor(rows, device=p.device)])
+    tol = P_TOL_BF16 if p.dtype == torch.bfloat16 else P_TOL_F32
+    assert float(np.max(np.abs(pg - P_ref))) <= tol
+
+
+def _run(x, p, lse, lse_only, stream=None):
+    fattn.softmax_rows(x, out=p, lse=lse, stream=stream)
+    fattn.logsumexp_rows(x, out=lse_only, stream=stream)
+
+
+def _fresh(x):
+    rows = x.shape[0]
+    return nan_full(x.shape, x.dtype), nan_full((rows,), torch.float32), nan_full((rows,), torch.float32)
+
+
+@pytest.mark.parametrize("rows,cols,din", SHAPES)
+def test_back_to_back_launches(rows, cols, din):
+    x_cpu = inputs.rows_inputs(rows, cols, din, seed=rows + cols, spike=12.0)
+    x = x_cpu.cuda()
+    outs = [_fresh(x) for _ in range(6)]
+    for o in outs:  # no synchronisation between the launches
+        _run(x, *o)
+    assert fattn.device_status() == fattn.FA_OK
+    _oracle_check(x_cpu, *outs[0])
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("rows,cols,din", SHAPES[:3])
+def test_graph_replays(rows, cols, din):
+    x_cpu = inputs.rows_inputs(rows, cols, din, seed=rows * 3 + cols)
+    x = x_cpu.cuda()
+    ref = _fresh(x)
+    _run(x, *ref)
+    assert fattn.device_status() == fattn.FA_OK
+    _oracle_check(x_cpu, *ref)
+    out = _fresh(x)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        _run(x, *out)  # the kernels' one-time set-up happens outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _run(x, *out)
+    for _ in range(6):
+        for t in out:
+            t.fill_(float("nan"))
+        g.replay()
+        assert fattn.device_status() == fattn.FA_OK
+        for a, b in zip(ref, out):
+            assert torch.equal(a, b)
+
+
+def test_streams_at_once():
+    shapes = [SHAPES[0], SHAPES[2], SHAPES[3], SHAPES[1]]
+    xs_cpu = [inputs.rows_inputs(r, c, d, seed=r + 7 * c) for r, c, d in shapes]
+    xs = [x.cuda() for x in xs_cpu]
+    streams = [torch.cuda.Stream() for _ in shapes]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    outs = [[_fresh(x) for _ in range(6)] for x in xs]
+    for k in range(6):  # interleaved, no synchronisation between the streams
+        for x, s, o in zip(xs, streams, outs):
+            with torch.cuda.stream(s):
+                _run(x, *o[k], stream=s)
+    for s in streams:
+        assert fattn.device_status(stream=s) == fattn.FA_OK
+    for x_cpu, o in zip(xs_cpu, outs):
+        _oracle_check(x_cpu, *o[0])
+        for other in o[1:]:
+            for a, b in zip(o[0], other):
+                assert torch.equal(a, b)
