@@ -462,7 +462,8 @@ static_assert(kRowq > kTmaMaxStages && kRowq % 4 == 0, "row index ring");
 // Under full load the SMs do not stream at one rate (the row count an SM gets
 // through in a fixed time varies by about +-8 %), so with a purely static
 // split the slowest SM's rows set the end of the kernel.  The LSE kernel on
-// rows above 16 KB therefore takes its first rounds of rows statically (row
+// rows above 16 KB and the softmax kernel on rows of 8-16 KB (where measured
+// faster) therefore take their first rounds of rows statically (row
 // blockIdx.x + j * gridDim.x) and the last kTailRounds rounds of 64 KB per CTA
 // a chunk of rows per request from a counter, so that the faster SMs take more
 // of the tail.
@@ -476,7 +477,7 @@ constexpr int kTailSlots = 256;
 constexpr int kTailRounds = 8;
 __device__ unsigned long long g_tail_ctr[kTailSlots];
 
-// The producer lane of the pipelined LSE kernel with tail rows: rows into the
+// The producer lane of the pipelined kernels with tail rows: rows into the
 // ring of `nst` stages (item i's row index in rowq[i % kRowq]), then one end
 // marker (row -1) per consumer group, so that every group's last item is its
 // marker.  `tail`: the launch's counter (null: a static split of every row).
@@ -562,10 +563,12 @@ __device__ __forceinline__ void produce_rows(const TIn* __restrict__ X, long row
 // PACKED: the slice stays packed until the exponent pass, which runs on
 // fp32 pairs (faster with four or more stages in the ring; with three, at
 // 64 KB rows, the unpacked form is).
-template <typename TIn, typename TOut, bool WRITE_P, int NV, bool LOGP, bool PACKED, int NG>
+// TAIL: the last rounds of rows come from the launch's counter `tail` (see
+// produce_rows); the ring then carries each item's row index.
+template <typename TIn, typename TOut, bool WRITE_P, int NV, bool LOGP, bool PACKED, int NG, bool TAIL>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restrict__ LSE, long rows, long cols,
-                 uint32_t stage_bytes, int nst, int* status) {
+                 uint32_t stage_bytes, int nst, int* status, unsigned long long* __restrict__ tail) {
     constexpr int V = Elem<TIn>::kVec;
     constexpr int W = kTmaConsumers / 32;
     constexpr int WG = W / NG;              // warps per group
@@ -598,8 +601,14 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
     }
     __syncthreads();
 
+    long long* rowq = reinterpret_cast<long long*>(gbase + (uint32_t)nst * stage_bytes + kTmaRowqOffset);
     if (warp == W) {
         // ------------------------------------------------ producer
+        if constexpr (TAIL) {
+            if (lane == 0)
+                produce_rows<TIn>(X, rows, cols, base, stage_bytes, nst, NG, bar0, rowq, abort_flag, status, tail);
+            return;
+        }
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();  // every row is read exactly once
             long issued = 0;
@@ -631,8 +640,10 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
     const int g = NG == 1 ? 0 : warp / WG;                              // consumer group
     const int gw = NG == 1 ? warp : warp % WG;                          // warp within the group
     const int gt = NG == 1 ? (int)threadIdx.x : (int)threadIdx.x % GT;  // thread within the group
-    // row i of this CTA is the group's (i / NG)-th
-    for (long i = g, r = blockIdx.x + (long)g * gridDim.x; r < rows; i += NG, r += (long)NG * gridDim.x) {
+    // item i of this CTA is the group's (i / NG)-th; static split: row
+    // blockIdx.x + i * gridDim.x; with TAIL the ring holds each item's row,
+    // and a row < 0 ends the group's work
+    for (long i = g, r = blockIdx.x + (long)g * gridDim.x; TAIL || r < rows; i += NG, r += (long)NG * gridDim.x) {
         const int s = (int)(i % nst);
         const uint32_t ph = (uint32_t)(i / nst) & 1u;
         bool ok = mbar_wait_bounded(full(s), ph, abort_flag, kWaitLimitNs);
@@ -642,6 +653,7 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
             atomicExch(status, kDevStatusTimeout);
             break;
         }
+        if (TAIL && rowq[i % kRowq] < 0) break;
         // the row slice into registers, then the stage goes back to the
         // producer; v becomes exp(x - m) for this thread's max m (log p keeps
         // x itself).  A slice that is all -inf (masked logits) takes m = 0 for
@@ -758,11 +770,12 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
                 merge_ms(M, S, m2, s2);
             }
         }
+        const long row = TAIL ? (long)rowq[i % kRowq] : r;
         if (WRITE_P) {
             // p = exp(x - m) * exp(m - M) / S;  log p = x - (M + ln S)
             const float f = m == -CUDART_INF_F ? 0.f : ex2((m - M) * kc) / S;
             const float lse_row = M + logf(S);
-            TOut* prow = P + r * cols;
+            TOut* prow = P + row * cols;
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
                 const long vi = gt + (long)k * GT;
@@ -774,7 +787,7 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
                 }
             }
         }
-        if (LSE != nullptr && gt == 0) LSE[r] = M + logf(S);
+        if (LSE != nullptr && gt == 0) LSE[row] = M + logf(S);
     }
 }
 
@@ -988,7 +1001,7 @@ int device_sms() {
 
 // Counter slots for the tail rows, per device: each CUDA stream (by its id,
 // which a context never reuses) gets a slot of its own the first time it
-// launches the LSE kernel with tail rows, and keeps it.  Launches on one stream run one
+// launches a pipelined kernel with tail rows, and keeps it.  Launches on one stream run one
 // after another, each starting with the word its predecessor zeroed, so a
 // slot never serves two launches at once.  Streams beyond kTailSlots keep the
 // static split.
@@ -1067,23 +1080,31 @@ bool try_launch_tma(const TIn* X, TOut* P, float* LSE, long rows, long cols, int
     nst -= nst % ng;  // stage s belongs to group s % ng
     const uint32_t smem = (uint32_t)nst * stage + kTmaSmemExtra;
     const long grid = rows < device_sms() ? rows : device_sms();
-    auto launch = [&](auto kern) {
+    auto launch = [&](auto kern, unsigned long long* tail) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess) {
-            kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(X, P, LSE, rows, cols, stage, nst, status);
+            kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(X, P, LSE, rows, cols, stage, nst, status, tail);
             e = cudaGetLastError();
         }
-        *err = e;
+        return e;
     };
-    if (ng == 4) {
-        if (nvec <= 4L * (kTmaConsumers / 4)) launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4, LOGP, true, 4>);
-        else launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, true, 4>);
+    if (ng == 4 && nvec <= 4L * (kTmaConsumers / 4)) {  // up to 8 KB
+        *err = launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4, LOGP, true, 4, false>, nullptr);
+    } else if (ng == 4) {
+        // rows of 8-16 KB: tail rows when the static rounds are at least half
+        // of every CTA's rows (shorter rows, and one group of 16 warps on
+        // longer ones: a static split measured as fast or faster)
+        const bool tail_ok = rows / grid >= 2L * kTailRounds * (65536 / row_bytes);
+        *err = launch_tail(st, tail_ok, rows, row_bytes, [&](unsigned long long* tail) {
+            return tail ? launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, true, 4, true>, tail)
+                        : launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, true, 4, false>, nullptr);
+        });
     } else if (nvec <= 4L * kTmaConsumers) {  // up to 32 KB: four stages
-        launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4, LOGP, true, 1>);
+        *err = launch(softmax_rows_tma<TIn, TOut, WRITE_P, 4, LOGP, true, 1, false>, nullptr);
     } else if (nst >= 4) {
-        launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, true, 1>);
+        *err = launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, true, 1, false>, nullptr);
     } else {
-        launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, false, 1>);
+        *err = launch(softmax_rows_tma<TIn, TOut, WRITE_P, 8, LOGP, false, 1, false>, nullptr);
     }
     return true;
 }
