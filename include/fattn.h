@@ -22,7 +22,12 @@
  *    FA_ERR_DEVICE_TIMEOUT in a per-device status word that
  *    fa_device_status() returns.
  *  - Re-entrant; the only global state is per-device kernel attributes, the
- *    device status word and a cache of encoded TMA tensor maps.
+ *    device status word, a cache of encoded TMA tensor maps and, for the row
+ *    kernels that hand their last rows out at run time, one counter word per
+ *    CUDA stream (256 per device, in the library's own device memory; the
+ *    launches on a stream run in order, each leaving its word zero for the
+ *    next; later streams, and launches into a stream capture, split their
+ *    rows statically).
  */
 #ifndef FATTN_H
 #define FATTN_H
