@@ -801,7 +801,8 @@ softmax_rows_tma(const TIn* __restrict__ X, TOut* __restrict__ P, float* __restr
 // stage, takes the slice max on the packed values and sums one exponential
 // per element relative to it.
 // NG consumer groups: two of 8 warps for rows above 16 KB, eight of 2 warps
-// (one stage each) for rows of 8-16 KB.
+// (one stage each) for rows of 8-16 KB.  NV: 16-byte vectors per thread (the
+// slots past the row end hold -inf).
 // TAIL: the last rounds of rows come from the launch's counter `tail` (see
 // produce_rows); the ring then carries each item's row index.
 template <typename TIn, int NV, int NG, bool TAIL>
@@ -1140,6 +1141,7 @@ bool try_launch_lse_tma(const TIn* X, float* LSE, long rows, long cols, int* sta
     if (ng == 8) {
         // (rows up to 16 KB: a static split measured faster)
         if (nvec <= 8L * (kTmaConsumers / 8)) *err = launch(logsumexp_rows_tma<TIn, 8, 8, false>, nullptr);
+        else if (nvec <= 12L * (kTmaConsumers / 8)) *err = launch(logsumexp_rows_tma<TIn, 12, 8, false>, nullptr);
         else *err = launch(logsumexp_rows_tma<TIn, 16, 8, false>, nullptr);
         return true;
     }

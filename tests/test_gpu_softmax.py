@@ -108,14 +108,16 @@ def test_cluster_rows(cols, din, dout):
 
 
 @pytest.mark.parametrize("rows", [64, 153, 1000])
-@pytest.mark.parametrize("cols,din", [(4096, torch.bfloat16), (6144, torch.bfloat16), (8192, torch.bfloat16),
+@pytest.mark.parametrize("cols,din", [(4096, torch.bfloat16), (4352, torch.bfloat16), (5000, torch.bfloat16),
+                                      (6144, torch.bfloat16), (8192, torch.bfloat16),
                                       (16384, torch.bfloat16), (24576, torch.bfloat16), (32768, torch.bfloat16),
                                       (2560, torch.float32), (4096, torch.float32), (16384, torch.float32)])
 @pytest.mark.parametrize("dout", [torch.bfloat16, torch.float32])
 def test_pipelined_rows(rows, cols, din, dout):
     # rows of 8-64 KB take the persistent pipelined kernel (four consumer
-    # groups up to 16 KB, some with part of each thread's slice past the row
-    # end); with more rows than SMs each CTA cycles its ring several times
+    # groups up to 16 KB, eight for the LSE alone, some with part of each
+    # thread's slice past the row end: 4352 and 5000 columns on 12 vectors per
+    # thread); with more rows than SMs each CTA cycles its ring several times
     x = inputs.rows_inputs(rows, cols, din, seed=rows + cols)
     p, lse = softmax(x.cuda(), out_dtype=dout)
     lse2 = logsumexp(x.cuda())
