@@ -13,7 +13,9 @@ launches back to back on one stream, for launches on four streams at once,
 and for the same calls captured once in a CUDA graph and replayed (a captured
 launch keeps the static split: the replays must still write every row, with
 the same bits as the direct launch); the first result of each case is
-compared with the fp64 oracle (LSE on every row, P on 64 sampled rows).
+compared with the fp64 oracle (LSE on every row, P on 64 sampled rows).  The
+fused cross-entropy (LSE kernel) and the log-softmax (softmax kernel) are
+checked with tail rows too.
 Tolerances as in the row softmax tests: P max-abs 4e-3 (bf16) / 1e-5 (fp32),
 LSE relative 1e-3.
 """
@@ -23,7 +25,8 @@ import torch
 
 import oracle
 from online_softmax_10_gb300 import fattn, inputs
-from parity import P_TOL_BF16, P_TOL_F32, ensure_built, lse_ok, nan_full, to_np
+from parity import (LSE_REL, P_TOL_BF16, P_TOL_F32, ensure_built, lse_ok, nan_full, rows_cross_entropy,
+                    rows_log_softmax, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -128,3 +131,43 @@ def test_streams_at_once():
         for other in o[1:]:
             for a, b in zip(o[0], other):
                 assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("rows,cols,din", [SHAPES[0], SHAPES[7]])
+def test_cross_entropy_with_tail_rows(rows, cols, din):
+    """The fused cross-entropy runs in the LSE kernel, so with tail rows the
+    loss and LSE of each row must come from that row's label (the row index
+    the ring carries), including ignored labels (-100, out of range)."""
+    x_cpu = inputs.rows_inputs(rows, cols, din, seed=rows + 3 * cols)
+    g = torch.Generator().manual_seed(rows)
+    labels = torch.randint(0, cols, (rows,), generator=g)
+    labels[::17] = -100
+    labels[5::23] = cols + 3
+    x, lab = x_cpu.cuda(), labels.cuda()
+    for _ in range(3):  # back to back: each launch takes the counter over
+        loss, lse = rows_cross_entropy(x, lab, want_lse=True)
+    assert fattn.device_status() == fattn.FA_OK
+    ref, L = oracle.cross_entropy_rows(x_cpu, labels)
+    lg = to_np(loss)
+    assert np.all(np.abs(lg - ref) <= LSE_REL * np.maximum(1.0, np.abs(ref))), float(np.max(np.abs(lg - ref)))
+    assert np.all(lg[labels.numpy() < 0] == 0)
+    ok, rel = lse_ok(to_np(lse), L)
+    assert ok, rel
+
+
+@pytest.mark.parametrize("rows,cols,din", [SHAPES[2], SHAPES[5]])
+def test_log_softmax_with_tail_rows(rows, cols, din):
+    """log p = x - LSE from the softmax kernel's log form with tail rows
+    (rows of 8-16 KB): every row written, sampled rows against the oracle."""
+    x_cpu = inputs.rows_inputs(rows, cols, din, seed=rows + 5 * cols)
+    x = x_cpu.cuda()
+    for _ in range(3):
+        y, lse = rows_log_softmax(x, out_dtype=torch.float32)
+    assert fattn.device_status() == fattn.FA_OK
+    assert not torch.isnan(y).any().item(), "a row was never written"
+    ok, rel = lse_ok(to_np(lse), oracle.logsumexp_rows(x_cpu))
+    assert ok, rel
+    sample = inputs.sample_rows(rows, P_SAMPLE, seed=cols).numpy()
+    Y, _ = oracle.log_softmax_rows(x_cpu[torch.as_tensor(sample)])
+    yg = to_np(y[torch.as_tensor(sample, device=y.device)])
+    assert np.all(np.abs(yg - Y) <= 1e-5 + 1e-6 * np.abs(Y)), float(np.max(np.abs(yg - Y)))
