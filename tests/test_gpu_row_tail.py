@@ -9,7 +9,9 @@ and the last CTA of a launch zeroes it for the next.
 A row's arithmetic does not depend on the CTA that computes it, so every
 launch of the same input must give the same bits, and every row must be
 written: outputs start as NaN, so a row that no CTA took fails.  Checked for
-launches back to back on one stream, for launches on four streams at once,
+launches back to back on one stream, for launches on four streams at once, on
+300 fresh streams at once (more than the 256 counters: the rest split
+statically),
 and for the same calls captured once in a CUDA graph and replayed (a captured
 launch keeps the static split: the replays must still write every row, with
 the same bits as the direct launch); the first result of each case is
@@ -19,6 +21,8 @@ checked with tail rows too.
 Tolerances as in the row softmax tests: P max-abs 4e-3 (bf16) / 1e-5 (fp32),
 LSE relative 1e-3.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -171,3 +175,46 @@ def test_log_softmax_with_tail_rows(rows, cols, din):
     Y, _ = oracle.log_softmax_rows(x_cpu[torch.as_tensor(sample)])
     yg = to_np(y[torch.as_tensor(sample, device=y.device)])
     assert np.all(np.abs(yg - Y) <= 1e-5 + 1e-6 * np.abs(Y)), float(np.max(np.abs(yg - Y)))
+
+
+class _RawStream:
+    """A CUDA stream handle in the form the binding takes (``.cuda_stream``)."""
+
+    def __init__(self, handle):
+        self.cuda_stream = handle
+
+
+def test_more_streams_than_counters():
+    """Each stream keeps the counter it got first; once the 256 counters of the
+    device are taken, further streams split their rows statically.  300 fresh
+    non-blocking streams (created through the driver API: the framework's own
+    stream objects come from a small pool), one launch on each, all in flight
+    together: every result the same bits, and equal to the oracle.  (Runs last
+    in this file: afterwards no new stream of this process gets a counter.)"""
+    try:
+        libcuda = ctypes.CDLL("libcuda.so.1")
+    except OSError:
+        pytest.skip("driver library not loadable")
+    rows, cols, din = SHAPES[0]
+    x_cpu = inputs.rows_inputs(rows, cols, din, seed=17)
+    x = x_cpu.cuda()
+    outs = [nan_full((rows,), torch.float32) for _ in range(300)]
+    torch.cuda.synchronize()  # inputs and outputs ready before the non-blocking streams run
+    handles = []
+    try:
+        for _ in range(300):
+            h = ctypes.c_void_p()
+            assert libcuda.cuStreamCreate(ctypes.byref(h), 1) == 0  # CU_STREAM_NON_BLOCKING
+            handles.append(h)
+        for h, o in zip(handles, outs):
+            fattn.logsumexp_rows(x, out=o, stream=_RawStream(h.value))
+        for h in handles:
+            assert libcuda.cuStreamSynchronize(h) == 0
+    finally:
+        for h in handles:
+            libcuda.cuStreamDestroy_v2(h)
+    assert fattn.device_status() == fattn.FA_OK
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    ok, rel = lse_ok(to_np(outs[0]), oracle.logsumexp_rows(x_cpu))
+    assert ok, rel
