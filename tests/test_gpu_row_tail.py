@@ -2,24 +2,22 @@
 
 Rows of 8-64 KB go through a persistent kernel with one CTA per SM.  The
 LSE-only kernel on rows above 16 KB and the softmax kernel on rows of 8-16 KB
-take their first rounds of rows statically and the last rounds a chunk of
-rows per request from a counter in device memory.  Each CUDA stream gets a
-counter of its own, so launches that share a counter run one after another,
-and the last CTA of a launch zeroes it for the next.
-A row's arithmetic does not depend on the CTA that computes it, so every
-launch of the same input must give the same bits, and every row must be
-written: outputs start as NaN, so a row that no CTA took fails.  Checked for
-launches back to back on one stream, for launches on four streams at once, on
-300 fresh streams at once (more than the 256 counters: the rest split
-statically),
-and for the same calls captured once in a CUDA graph and replayed (a captured
-launch keeps the static split: the replays must still write every row, with
-the same bits as the direct launch); the first result of each case is
-compared with the fp64 oracle (LSE on every row, P on 64 sampled rows).  The
-fused cross-entropy (LSE kernel) and the log-softmax (softmax kernel) are
-checked with tail rows too.
-Tolerances as in the row softmax tests: P max-abs 4e-3 (bf16) / 1e-5 (fp32),
-LSE relative 1e-3.
+take their first rounds of rows statically and the last rounds a chunk of rows
+per request from a counter in device memory.  Each CUDA stream gets a counter
+of its own, so launches that share a counter run one after another, and the
+last CTA of a launch zeroes it for the next.  A row's arithmetic does not
+depend on the CTA that computes it, so every launch of the same input must
+give the same bits, and every row must be written: outputs start as NaN, so a
+row that no CTA took fails.  Checked for launches back to back on one stream,
+for launches on four streams at once, on 300 fresh streams at once (more than
+the 256 counters: the rest split statically), and for the same calls captured
+once in a CUDA graph and replayed (a captured launch keeps the static split:
+the replays must still write every row, with the same bits as the direct
+launch); the first result of each case is compared with the fp64 oracle (LSE
+on every row, P on 64 sampled rows).  The fused cross-entropy (LSE kernel) and
+the log-softmax (softmax kernel) are checked with tail rows too.  Tolerances
+as in the row softmax tests: P max-abs 4e-3 (bf16) / 1e-5 (fp32), LSE relative
+1e-3.
 """
 import ctypes
 
